@@ -1,0 +1,389 @@
+"""CPU oracle for the CODA GEMM-plus-epilogue block: plain, slow, fp64.
+
+TEST INFRASTRUCTURE ONLY. Only the test suite, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import or run this module. The CUDA
+library never calls it, and it shares no code with the CUDA library: it
+computes everything from the plain definitions, with numpy matmul as the only
+library step.
+
+Sources (the pages' titles and sections):
+  [pith]   "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
+           (pith.science summary of arXiv 2605.19269): Fig. 4 and Fig. 5
+           captions (GEMM-RMSNorm-GEMM, r = 1/sqrt(reduce(r_hat) + eps)),
+           Fig. 7 caption (pairwise maps), Appendix A.1 "Tile-wise Epilogue",
+           Listing 2 "Kernel Example" (residual + mean-of-squares + RMSNorm
+           weight epilogue).
+  [notes]  "Reading notes on CODA" (jianyuh.github.io): section 2
+           "Forward-Pass Reparameterizations" (GEMM -> Residual -> RMSNorm ->
+           GEMM; pairwise activations; cross-entropy loss), section 3 "The
+           Backward Pass: Reverse Fusion" (including "Eliminating the RMSNorm
+           backward kernel").
+  [thread] digg thread on CODA: Patterns 1-3 and the commutation identity.
+
+Two forms are kept:
+  * canonical  -- the block as frameworks write it (RMSNorm applied before the
+                  second GEMM, autograd-by-hand backward). This is the
+                  reference every GPU result is compared with.
+  * reparam    -- the pages' rewritten form (delayed row scale r, statistic s
+                  from (grad y, y)). It must equal the canonical form in exact
+                  arithmetic; with ``store_bf16=True`` it also rounds, to bf16,
+                  the tensors that the rewritten kernels write to memory, which
+                  models the storage precision of the fused path.
+
+Parity status: every function here is pinned by the CPU tests in
+tests/test_oracle_*.py (closed forms, invariants, finite differences, torch
+library special cases, brute force on tiny inputs). The relative-error study
+of the pages' Fig. 6 is not reproduced (no values are printed): parity
+unpinned for that comparison only.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional
+
+import numpy as np
+
+EPS = 1e-6          # RMSNorm epsilon, inside the square root
+ROPE_THETA = 500000.0
+
+f64 = np.float64
+
+
+# --------------------------------------------------------------------------
+# storage rounding
+# --------------------------------------------------------------------------
+
+def bf16_round(a) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 value (ties to even), returned
+    as fp64. bf16 keeps 8 significant bits; fp64 has 53, so the low 45 bits
+    of the fp64 significand are rounded away. Below 2^-126 bf16 is
+    subnormal with a fixed spacing of 2^-133."""
+    a = np.ascontiguousarray(np.asarray(a, dtype=f64))
+    u = a.view(np.uint64)
+    lsb = (u >> np.uint64(45)) & np.uint64(1)
+    bias = np.uint64((1 << 44) - 1) + lsb
+    mask = np.uint64(~((1 << 45) - 1) & 0xFFFFFFFFFFFFFFFF)
+    r = ((u + bias) & mask).view(f64)
+    tiny = np.abs(a) < 2.0 ** -126
+    if np.any(tiny):
+        r = np.where(tiny, np.round(a * 2.0 ** 133) * 2.0 ** -133, r)
+    return r
+
+
+def _store(store_bf16: bool):
+    return bf16_round if store_bf16 else (lambda t: t)
+
+
+# --------------------------------------------------------------------------
+# elementwise maps
+# --------------------------------------------------------------------------
+
+def sigmoid(t):
+    t = np.asarray(t, dtype=f64)
+    return 1.0 / (1.0 + np.exp(-t))
+
+
+def silu(t):
+    """silu(t) = t * sigmoid(t) (the SwiGLU gate activation)."""
+    t = np.asarray(t, dtype=f64)
+    return t * sigmoid(t)
+
+
+def silu_grad(t):
+    """d silu / dt = sigmoid(t) * (1 + t * (1 - sigmoid(t)))."""
+    t = np.asarray(t, dtype=f64)
+    s = sigmoid(t)
+    return s * (1.0 + t * (1.0 - s))
+
+
+def rms_factor(h, eps: float = EPS):
+    """Row-wise inverse RMS: r = 1 / sqrt(mean_j h_j^2 + eps)  [notes s2;
+    pith Fig. 5 caption: eps inside the square root]."""
+    h = np.asarray(h, dtype=f64)
+    return 1.0 / np.sqrt(np.mean(h * h, axis=1) + eps)
+
+
+def swiglu(y):
+    """Pairwise SwiGLU on gate/up-interleaved columns: column 2k is gate g_k,
+    column 2k+1 is up u_k, output a_k = silu(g_k) * u_k  [pith Fig. 7
+    caption; notes s2 "Pairwise activations"]."""
+    g = y[:, 0::2]
+    u = y[:, 1::2]
+    return silu(g) * u
+
+
+# --------------------------------------------------------------------------
+# MLP block: GEMM -> residual -> RMSNorm -> GEMM -> SwiGLU -> GEMM
+# --------------------------------------------------------------------------
+
+def mlp_fwd(x, z, W0, W1, W2, gamma, eps: float = EPS) -> Dict[str, np.ndarray]:
+    """Canonical forward [notes s2 "GEMM -> Residual -> RMSNorm -> GEMM"]:
+        h  = x W0 + z
+        r  = 1/sqrt(mean(h^2) + eps)
+        n  = r h ;  h2 = n * gamma
+        y  = h2 W1 ;  a = silu(y[:,0::2]) * y[:,1::2]
+        out = a W2
+    """
+    x, z, W0, W1, W2, gamma = (np.asarray(t, dtype=f64) for t in (x, z, W0, W1, W2, gamma))
+    h = x @ W0 + z
+    r = rms_factor(h, eps)
+    n = r[:, None] * h
+    h2 = n * gamma[None, :]
+    y = h2 @ W1
+    a = swiglu(y)
+    out = a @ W2
+    return {"h": h, "r": r, "n": n, "h2": h2, "y": y, "a": a, "out": out}
+
+
+def mlp_fwd_reparam(x, z, W0, W1, W2, gamma, eps: float = EPS,
+                    store_bf16: bool = False) -> Dict[str, np.ndarray]:
+    """The pages' rewritten forward [notes s2; pith Fig. 4; thread Pattern 1]:
+        GEMM 1 epilogue: h = x W0 + z (stored), hg = h * gamma (stored),
+                         row statistic from the unscaled h (Listing 2: the
+                         mean of squares is taken on D before the RMSNorm
+                         weight multiplies it)
+        auxiliary:       r = 1/sqrt(mean(h^2) + eps)
+        GEMM 2 epilogue: y = r * (hg W1)  (delayed row scale, stored),
+                         a = silu(y_gate) * y_up (stored)
+        GEMM 3:          out = a W2
+    With store_bf16, each stored tensor is rounded to bf16 where the rewritten
+    kernels write it; its consumers read the rounded value, the statistics are
+    taken before rounding."""
+    st = _store(store_bf16)
+    x, z, W0, W1, W2, gamma = (np.asarray(t, dtype=f64) for t in (x, z, W0, W1, W2, gamma))
+    h_acc = x @ W0 + z
+    r = rms_factor(h_acc, eps)
+    h = st(h_acc)
+    hg = st(h_acc * gamma[None, :])
+    y_acc = r[:, None] * (hg @ W1)
+    a = st(swiglu(y_acc))
+    y = st(y_acc)
+    out = st(a @ W2)
+    return {"h": h, "r": r, "hg": hg, "y": y, "a": a, "out": out}
+
+
+def mlp_bwd(fwd: Dict[str, np.ndarray], x, W0, W1, W2, gamma, dout) -> Dict[str, np.ndarray]:
+    """Canonical backward of ``mlp_fwd`` for the scalar L = sum(dout * out),
+    written out by hand (chain rule through each op in turn):
+        da  = dout W2^T ;          dW2 = a^T dout
+        dg  = da * u * silu'(g) ;  du = da * silu(g) ;  dy = interleave(dg, du)
+        dW1 = h2^T dy ;            dh2 = dy W1^T
+        dgamma = sum_rows dh2 * n ;  dn = gamma * dh2
+        s   = mean_j(dn * n)      (equals (1/d) sumcols(dh2 * h2), notes s3)
+        dh  = r (dn - s n)        (RMSNorm backward)
+        dz  = dh ;  dx = dh W0^T ;  dW0 = x^T dh
+    """
+    x, W0, W1, W2, gamma, dout = (np.asarray(t, dtype=f64) for t in (x, W0, W1, W2, gamma, dout))
+    h, r, n, h2, y, a = (fwd[k] for k in ("h", "r", "n", "h2", "y", "a"))
+    d = h.shape[1]
+    da = dout @ W2.T
+    dW2 = a.T @ dout
+    g = y[:, 0::2]
+    u = y[:, 1::2]
+    dy = np.empty_like(y)
+    dy[:, 0::2] = da * u * silu_grad(g)
+    dy[:, 1::2] = da * silu(g)
+    dW1 = h2.T @ dy
+    dh2 = dy @ W1.T
+    dgamma = np.sum(dh2 * n, axis=0)
+    dn = gamma[None, :] * dh2
+    s = np.sum(dn * n, axis=1) / d
+    dh = r[:, None] * (dn - s[:, None] * n)
+    dx = dh @ W0.T
+    dW0 = x.T @ dh
+    return {"da": da, "dy": dy, "dh2": dh2, "s": s, "dh": dh, "dz": dh, "dx": dx,
+            "dW0": dW0, "dW1": dW1, "dW2": dW2, "dgamma": dgamma}
+
+
+def mlp_bwd_reparam(fwd: Dict[str, np.ndarray], x, W0, W1, W2, gamma, dout,
+                    store_bf16: bool = False) -> Dict[str, np.ndarray]:
+    """The pages' reverse-fused backward [notes s3 "Reverse Fusion" and
+    "Eliminating the RMSNorm backward kernel"], on the tensors saved by
+    ``mlp_fwd_reparam`` (h, hg, r, y, a):
+        GEMM (dout W2^T) epilogue: f'(h) multiplies into the gradient GEMM:
+            dg = da * u * silu'(g), du = da * silu(g)  (one incoming gradient,
+            two outgoing: the SwiGLU backward pairwise map, pith Fig. 7),
+            s-partial = sum_j dy_j * y_j, stored dyhat = r * dy
+        auxiliary: s = (1/d) sumcols(dy * y)
+        GEMM (dyhat W1^T) epilogue: P = r dh2;  dh = gamma * P - r^2 s h ;
+            dgamma = sum_rows P * h
+        dW1 = hg^T dyhat ; dW2 = a^T dout ; dx = dh W0^T ; dW0 = x^T dh
+    """
+    st = _store(store_bf16)
+    x, W0, W1, W2, gamma, dout = (np.asarray(t, dtype=f64) for t in (x, W0, W1, W2, gamma, dout))
+    h, hg, r, y, a = (fwd[k] for k in ("h", "hg", "r", "y", "a"))
+    d = h.shape[1]
+    da = dout @ W2.T
+    g = y[:, 0::2]
+    u = y[:, 1::2]
+    dy = np.empty_like(y)
+    dy[:, 0::2] = da * u * silu_grad(g)
+    dy[:, 1::2] = da * silu(g)
+    s = np.sum(dy * y, axis=1) / d
+    dyhat = st(r[:, None] * dy)
+    P = dyhat @ W1.T
+    dh = st(gamma[None, :] * P - (r * r * s)[:, None] * h)
+    dgamma = np.sum(P * h, axis=0)
+    dW1 = hg.T @ dyhat
+    dW2 = a.T @ dout
+    dx = st(dh @ W0.T)
+    dW0 = x.T @ dh
+    return {"dy": dy, "dyhat": dyhat, "s": s, "P": P, "dh": dh, "dz": dh, "dx": dx,
+            "dW0": dW0, "dW1": dW1, "dW2": dW2, "dgamma": dgamma}
+
+
+# --------------------------------------------------------------------------
+# RoPE on adjacent pairs
+# --------------------------------------------------------------------------
+
+def rope_inv_freq(head_dim: int, theta: float = ROPE_THETA) -> np.ndarray:
+    """theta_i = theta^(-2i/head_dim), i = 0 .. head_dim/2 - 1."""
+    i = np.arange(head_dim // 2, dtype=f64)
+    return np.power(f64(theta), -2.0 * i / head_dim)
+
+
+def rope_cos_sin(pos, head_dim: int, theta: float = ROPE_THETA):
+    """cos and sin of angle[p, i] = pos[p] * theta_i, in fp64."""
+    ang = np.asarray(pos, dtype=f64)[:, None] * rope_inv_freq(head_dim, theta)[None, :]
+    return np.cos(ang), np.sin(ang)
+
+
+def rope_apply(v, pos, n_rope_cols: int, head_dim: int, theta: float = ROPE_THETA,
+               inverse: bool = False) -> np.ndarray:
+    """Rotate each adjacent feature pair (2i, 2i+1) inside every head_dim-wide
+    head of the first n_rope_cols columns by angle pos * theta_i (pith Fig. 7:
+    RoPE rotates each feature pair and returns two outputs):
+        v'_{2i}   = v_{2i} cos - v_{2i+1} sin
+        v'_{2i+1} = v_{2i} sin + v_{2i+1} cos
+    Columns from n_rope_cols on are returned unchanged. ``inverse`` rotates by
+    the negative angle (the transpose of the rotation)."""
+    v = np.array(v, dtype=f64, copy=True)
+    c, s = rope_cos_sin(pos, head_dim, theta)
+    if inverse:
+        s = -s
+    nh = n_rope_cols // head_dim
+    for hidx in range(nh):
+        base = hidx * head_dim
+        e = v[:, base:base + head_dim:2].copy()
+        o = v[:, base + 1:base + head_dim:2].copy()
+        v[:, base:base + head_dim:2] = e * c - o * s
+        v[:, base + 1:base + head_dim:2] = e * s + o * c
+    return v
+
+
+# --------------------------------------------------------------------------
+# LM head + cross-entropy
+# --------------------------------------------------------------------------
+
+def lmhead_ce(hidden, W, targets) -> Dict[str, np.ndarray]:
+    """Per-token loss l_i = -h_{i,y_i} + log sum_k exp(h_{i,k}) on logits
+    h = hidden W [notes s2 "Cross-entropy loss"]; natural log, no reduction.
+    The log-sum-exp is taken with the row maximum factored out."""
+    hidden = np.asarray(hidden, dtype=f64)
+    W = np.asarray(W, dtype=f64)
+    t = np.asarray(targets, dtype=np.int64)
+    logits = hidden @ W
+    m = np.max(logits, axis=1)
+    lse = m + np.log(np.sum(np.exp(logits - m[:, None]), axis=1))
+    tl = logits[np.arange(logits.shape[0]), t]
+    return {"lse": lse, "loss": lse - tl, "target_logit": tl}
+
+
+def lse_two_level(logits, tile: int) -> np.ndarray:
+    """The pages' two-level log-sum-exp [notes s2 "Cross-entropy loss";
+    thread Pattern 3]: each column tile j keeps its own (max m_j, sum-exp
+    s_j = sum exp(l - m_j)); an auxiliary step combines them as
+    M = max_j m_j, LSE = M + log sum_j s_j exp(m_j - M)."""
+    logits = np.asarray(logits, dtype=f64)
+    V = logits.shape[1]
+    ms, ss = [], []
+    for c0 in range(0, V, tile):
+        blk = logits[:, c0:c0 + tile]
+        mj = np.max(blk, axis=1)
+        ms.append(mj)
+        ss.append(np.sum(np.exp(blk - mj[:, None]), axis=1))
+    ms = np.stack(ms, axis=1)
+    ss = np.stack(ss, axis=1)
+    Mx = np.max(ms, axis=1)
+    return Mx + np.log(np.sum(ss * np.exp(ms - Mx[:, None]), axis=1))
+
+
+# --------------------------------------------------------------------------
+# Llama-3-8B-shaped non-attention block (output projection .. QKV + RoPE)
+# --------------------------------------------------------------------------
+
+def block8b_fwd(o, z, Wo, W1, W2, gamma2, gamma1, Wqkv, pos, n_rope_cols: int,
+                head_dim: int, theta: float = ROPE_THETA, eps: float = EPS):
+    """Canonical forward of the non-attention part of a layer, with the
+    attention output o given:
+        h   = o Wo + z                       (output projection + residual)
+        n   = rmsnorm(h) ; h2 = n * gamma2
+        y   = h2 W1 ; a = silu(g) * u        (SwiGLU MLP)
+        out = a W2 + h                       (down projection + residual)
+        n'  = rmsnorm(out) ; q_in = n' * gamma1
+        qkv = RoPE(q_in Wqkv) on the q and k columns
+    """
+    o, z, Wo, W1, W2, gamma2, gamma1, Wqkv = (np.asarray(t, dtype=f64) for t in
+                                               (o, z, Wo, W1, W2, gamma2, gamma1, Wqkv))
+    h = o @ Wo + z
+    r = rms_factor(h, eps)
+    n = r[:, None] * h
+    h2 = n * gamma2[None, :]
+    y = h2 @ W1
+    a = swiglu(y)
+    out = a @ W2 + h
+    r1 = rms_factor(out, eps)
+    n1 = r1[:, None] * out
+    q_in = n1 * gamma1[None, :]
+    qkv_pre = q_in @ Wqkv
+    qkv = rope_apply(qkv_pre, pos, n_rope_cols, head_dim, theta)
+    return {"h": h, "r": r, "n": n, "h2": h2, "y": y, "a": a, "out": out, "r1": r1,
+            "n1": n1, "q_in": q_in, "qkv_pre": qkv_pre, "qkv": qkv}
+
+
+def block8b_bwd(fwd, o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres, pos,
+                n_rope_cols: int, head_dim: int, theta: float = ROPE_THETA):
+    """Canonical backward of ``block8b_fwd`` for L = sum(dqkv * qkv) +
+    sum(dres * out), written out by hand."""
+    o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres = (
+        np.asarray(t, dtype=f64) for t in (o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres))
+    d = fwd["h"].shape[1]
+    dqkv_pre = rope_apply(dqkv, pos, n_rope_cols, head_dim, theta, inverse=True)
+    dWqkv = fwd["q_in"].T @ dqkv_pre
+    dq_in = dqkv_pre @ Wqkv.T
+    dgamma1 = np.sum(dq_in * fwd["n1"], axis=0)
+    dn1 = gamma1[None, :] * dq_in
+    s1 = np.sum(dn1 * fwd["n1"], axis=1) / d
+    dout = fwd["r1"][:, None] * (dn1 - s1[:, None] * fwd["n1"]) + dres
+    da = dout @ W2.T
+    dW2 = fwd["a"].T @ dout
+    y = fwd["y"]
+    g = y[:, 0::2]
+    u = y[:, 1::2]
+    dy = np.empty_like(y)
+    dy[:, 0::2] = da * u * silu_grad(g)
+    dy[:, 1::2] = da * silu(g)
+    dW1 = fwd["h2"].T @ dy
+    dh2 = dy @ W1.T
+    dgamma2 = np.sum(dh2 * fwd["n"], axis=0)
+    dn = gamma2[None, :] * dh2
+    s = np.sum(dn * fwd["n"], axis=1) / d
+    dh = fwd["r"][:, None] * (dn - s[:, None] * fwd["n"]) + dout
+    do = dh @ Wo.T
+    dWo = o.T @ dh
+    return {"dqkv_pre": dqkv_pre, "dWqkv": dWqkv, "dgamma1": dgamma1, "s1": s1,
+            "dout": dout, "da": da, "dW2": dW2, "dy": dy, "dW1": dW1, "dgamma2": dgamma2,
+            "s": s, "dh": dh, "dz": dh, "do": do, "dWo": dWo}
+
+
+def to64(t) -> np.ndarray:
+    """Convert a torch tensor or array-like (e.g. bf16 inputs) to fp64 numpy."""
+    if hasattr(t, "detach"):
+        import torch  # local: only for the dtype conversion of inputs
+        return t.detach().to(torch.float64).cpu().numpy()
+    return np.asarray(t, dtype=f64)
+
+
+def lse_closed_form_zero_weights(V: int) -> float:
+    """With W = 0 every logit is 0, so LSE = log V and loss = log V."""
+    return math.log(V)

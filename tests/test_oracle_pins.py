@@ -1,0 +1,440 @@
+"""Pins for the CPU oracle (no GPU): closed forms, hand-worked examples,
+invariants, finite differences and torch library special cases. Each check is
+independent of the oracle's own code path, so a dropped term, a wrong sign or
+index, or a transposed operand in the oracle fails at least one of them
+(test_planted_mistakes_are_caught plants some and checks exactly that)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import coda_oracle as O
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))
+
+
+def rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+def rand_block(M=3, d=8, f=8, seed=0, wscale=0.3):
+    rng = np.random.default_rng(seed)
+    return dict(x=rng.standard_normal((M, d)), z=rng.standard_normal((M, d)),
+                W0=rng.standard_normal((d, d)) * wscale, W1=rng.standard_normal((d, 2 * f)) * wscale,
+                W2=rng.standard_normal((f, d)) * wscale, gamma=rng.uniform(0.5, 1.5, d),
+                dout=rng.standard_normal((M, d)))
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_bf16_round_matches_torch_on_fp32_values():
+    # torch's float32 -> bfloat16 conversion is round-to-nearest-even; on values
+    # that are exact in fp32 the oracle's fp64 rounding must agree with it.
+    rng = np.random.default_rng(1)
+    v = (rng.standard_normal(200000) * np.exp(rng.uniform(-30, 30, 200000))).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.bf16_round(v.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_round_ties_to_even_and_nearest():
+    one = 1.0
+    ulp = 2.0 ** -7
+    assert O.bf16_round(one + ulp / 2) == one                 # tie -> even (down)
+    assert O.bf16_round(one + 3 * ulp / 2) == one + 2 * ulp   # tie -> even (up)
+    assert O.bf16_round(one + ulp / 2 + 2 ** -30) == one + ulp
+    assert O.bf16_round(-(one + ulp / 2 + 2 ** -30)) == -(one + ulp)
+    # nearest: no other bf16 neighbour is closer
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal(10000) * 7.3
+    r = O.bf16_round(x)
+    e = np.floor(np.log2(np.abs(r)))
+    step = 2.0 ** (e - 7)
+    assert np.all(np.abs(x - r) <= step / 2 * (1 + 1e-12) + 1e-300)
+
+
+# ---------------------------------------------------------------- elementwise
+
+def test_silu_closed_forms():
+    for k, v in GOLD["silu"].items():
+        assert abs(O.silu(float(k)) - v) < 1e-15
+    for k, v in GOLD["dsilu"].items():
+        assert abs(O.silu_grad(float(k)) - v) < 1e-15
+    assert O.silu(0.0) == 0.0
+
+
+def test_silu_grad_finite_difference():
+    t = np.linspace(-8, 8, 101)
+    hstep = 1e-6
+    fd = (O.silu(t + hstep) - O.silu(t - hstep)) / (2 * hstep)
+    assert np.max(np.abs(fd - O.silu_grad(t))) < 1e-8
+
+
+def test_silu_matches_torch():
+    t = np.linspace(-20, 20, 4001)
+    assert rel(O.silu(t), F.silu(torch.from_numpy(t)).numpy()) < 1e-15
+
+
+# ---------------------------------------------------------------- MLP block
+
+def test_block_worked_example():
+    g = GOLD["block_example"]
+    i = g["inputs"]
+    arr = lambda k: np.array(i[k], dtype=np.float64)
+    x, z = arr("x")[None, :], arr("z")[None, :]
+    fw = O.mlp_fwd(x, z, arr("W0"), arr("W1"), arr("W2"), arr("gamma"), eps=i["eps"])
+    assert rel(fw["h"][0], g["h"]) < 1e-15
+    assert abs(fw["r"][0] - g["r"]) < 1e-15
+    assert rel(fw["y"][0], g["y"]) < 1e-14
+    assert abs(fw["a"][0, 0] - g["a"]) < 1e-15
+    assert rel(fw["out"][0], g["out"]) < 1e-14
+    bw = O.mlp_bwd(fw, x, arr("W0"), arr("W1"), arr("W2"), arr("gamma"), arr("dout")[None, :])
+    assert abs(bw["s"][0] - g["s"]) < 1e-14
+    assert rel(bw["dy"][0], g["dy"]) < 1e-14
+    assert rel(bw["dh"][0], g["dh"]) < 1e-13
+    assert rel(bw["dgamma"], g["dgamma"]) < 1e-14
+    assert rel(bw["dW0"], g["dW0"]) < 1e-13
+    assert rel(bw["dW1"], g["dW1"]) < 1e-14
+    assert rel(bw["dW2"], g["dW2"]) < 1e-14
+
+
+def test_rms_factor_special_case_identity_weights():
+    # W0 = I, z = 0: h = x, so r = 1/sqrt(mean(x^2) + eps) with eps inside the sqrt.
+    rng = np.random.default_rng(3)
+    d = 16
+    x = rng.standard_normal((5, d))
+    fw = O.mlp_fwd(x, np.zeros_like(x), np.eye(d), rng.standard_normal((d, 8)),
+                   rng.standard_normal((4, d)), np.ones(d), eps=1e-6)
+    for m in range(5):
+        want = 1.0 / math.sqrt(sum(v * v for v in x[m]) / d + 1e-6)
+        assert abs(fw["r"][m] - want) < 1e-15 * want
+    # and with gamma = 1 the normalised rows have mean square mean/(mean+eps)
+    ms = np.mean(fw["h2"] ** 2, axis=1)
+    mx = np.mean(x * x, axis=1)
+    assert np.allclose(ms, mx / (mx + 1e-6), rtol=1e-14)
+
+
+def test_swiglu_zero_gate_and_limits():
+    y = np.zeros((2, 8))
+    y[:, 1::2] = 5.0
+    assert np.all(O.swiglu(y) == 0.0)            # g = 0 -> a = 0 whatever u is
+    y = np.zeros((1, 2))
+    y[0] = [40.0, 2.0]                           # silu(40) = 40 to fp64 precision
+    assert abs(O.swiglu(y)[0, 0] - 80.0) < 1e-12
+    y[0] = [-40.0, 2.0]
+    assert abs(O.swiglu(y)[0, 0]) < 1e-15
+
+
+def _block_torch(inp, eps=1e-6):
+    """Library special case: torch fp64 composition of rms_norm, silu and
+    matmul, differentiated by autograd."""
+    t = {k: torch.tensor(v, dtype=torch.float64, requires_grad=k != "dout") for k, v in inp.items()}
+    h = t["x"] @ t["W0"] + t["z"]
+    h2 = F.rms_norm(h, (h.shape[1],), t["gamma"], eps)
+    y = h2 @ t["W1"]
+    a = F.silu(y[:, 0::2]) * y[:, 1::2]
+    out = a @ t["W2"]
+    (out * t["dout"]).sum().backward()
+    return out.detach().numpy(), {k: t[k].grad.numpy() for k in ("x", "z", "W0", "W1", "W2", "gamma")}
+
+
+def test_block_matches_torch_autograd():
+    inp = rand_block(M=5, d=16, f=12, seed=4)
+    out_t, grads_t = _block_torch(inp)
+    fw = O.mlp_fwd(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"])
+    bw = O.mlp_bwd(fw, inp["x"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"], inp["dout"])
+    assert rel(fw["out"], out_t) < 1e-13
+    names = {"x": "dx", "z": "dz", "W0": "dW0", "W1": "dW1", "W2": "dW2", "gamma": "dgamma"}
+    for k, v in names.items():
+        assert rel(bw[v], grads_t[k]) < 1e-12, k
+
+
+def fd_block_error(inp, step=1e-6):
+    """Largest relative error, over every input, between the oracle's
+    gradients and central finite differences of L = sum(dout * out)."""
+    keys = ("x", "z", "W0", "W1", "W2", "gamma")
+
+    def loss(vals):
+        fw = O.mlp_fwd(vals["x"], vals["z"], vals["W0"], vals["W1"], vals["W2"], vals["gamma"])
+        return float(np.sum(fw["out"] * inp["dout"]))
+
+    fw = O.mlp_fwd(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"])
+    bw = O.mlp_bwd(fw, inp["x"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"], inp["dout"])
+    gname = {"x": "dx", "z": "dz", "W0": "dW0", "W1": "dW1", "W2": "dW2", "gamma": "dgamma"}
+    worst = 0.0
+    for k in keys:
+        base = inp[k]
+        fd = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            vals = {kk: inp[kk].copy() for kk in keys}
+            vals[k][idx] += step
+            lp = loss(vals)
+            vals[k][idx] -= 2 * step
+            lm = loss(vals)
+            fd[idx] = (lp - lm) / (2 * step)
+        worst = max(worst, rel(bw[gname[k]], fd))
+    return worst
+
+
+def test_block_backward_finite_differences():
+    inp = rand_block(M=2, d=8, f=8, seed=5)
+    assert fd_block_error(inp) < 1e-6
+
+
+def test_reparam_equals_canonical():
+    # commutation: r((xW0+z)*gamma)W1 = r(((xW0+z)*gamma)W1)  (exact arithmetic)
+    inp = rand_block(M=7, d=24, f=16, seed=6)
+    fc = O.mlp_fwd(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"])
+    fr = O.mlp_fwd_reparam(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"])
+    for k in ("h", "r", "y", "a", "out"):
+        assert rel(fr[k], fc[k]) < 1e-12, k
+    assert rel(fr["hg"] * fr["r"][:, None], fc["h2"]) < 1e-13
+    bc = O.mlp_bwd(fc, inp["x"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"], inp["dout"])
+    br = O.mlp_bwd_reparam(fr, inp["x"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"], inp["dout"])
+    for k in ("s", "dh", "dx", "dW0", "dW1", "dW2", "dgamma"):
+        assert rel(br[k], bc[k]) < 1e-11, k
+
+
+def test_s_two_forms_agree():
+    # s = (1/d) sumcols(dh2 * h2) = (1/d) sumcols(dy * y)  (notes s3)
+    inp = rand_block(M=6, d=20, f=10, seed=7)
+    fc = O.mlp_fwd(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"])
+    bc = O.mlp_bwd(fc, inp["x"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"], inp["dout"])
+    d = inp["x"].shape[1]
+    s1 = np.sum(bc["dh2"] * fc["h2"], axis=1) / d
+    s2 = np.sum(bc["dy"] * fc["y"], axis=1) / d
+    assert rel(s1, s2) < 1e-12
+    assert rel(bc["s"], s1) < 1e-12
+
+
+def test_storage_rounded_mode_rounds_stored_tensors_only():
+    inp = rand_block(M=4, d=16, f=8, seed=8)
+    fr = O.mlp_fwd_reparam(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"],
+                           store_bf16=True)
+    for k in ("h", "hg", "y", "a", "out"):
+        assert np.array_equal(fr[k], O.bf16_round(fr[k])), k
+    fe = O.mlp_fwd_reparam(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"])
+    assert rel(fr["r"], fe["r"]) < 1e-15          # statistics come from the unrounded h
+    assert rel(fr["out"], fe["out"]) < 2e-2
+
+
+# ---------------------------------------------------------------- cross-entropy
+
+def test_ce_zero_weights_closed_form():
+    V = 128256
+    hidden = np.random.default_rng(9).standard_normal((2, 4))
+    res = O.lmhead_ce(hidden, np.zeros((4, V)), np.array([0, V - 1]))
+    assert np.allclose(res["lse"], GOLD["ln_V_128256"], rtol=0, atol=1e-12)
+    assert np.allclose(res["loss"], GOLD["ln_V_128256"], rtol=0, atol=1e-12)
+
+
+def test_ce_small_closed_form():
+    W = np.array([[0.0, math.log(2), math.log(3), 0.0]])
+    res = O.lmhead_ce(np.ones((2, 1)), W, np.array([2, 0]))
+    g = GOLD["ce_small"]
+    assert abs(res["lse"][0] - g["lse"]) < 1e-15
+    assert abs(res["loss"][0] - g["loss_target2"]) < 1e-15
+    assert abs(res["loss"][1] - g["loss_target0"]) < 1e-15
+
+
+def test_ce_brute_force_and_torch():
+    rng = np.random.default_rng(10)
+    hidden = rng.standard_normal((6, 5))
+    W = rng.standard_normal((5, 37)) * 2.0
+    t = rng.integers(0, 37, 6)
+    res = O.lmhead_ce(hidden, W, t)
+    for i in range(6):
+        logits = [sum(hidden[i, k] * W[k, j] for k in range(5)) for j in range(37)]
+        lse = math.log(sum(math.exp(v) for v in logits))
+        assert abs(res["lse"][i] - lse) < 1e-12
+        assert abs(res["loss"][i] - (lse - logits[t[i]])) < 1e-12
+    ref = F.cross_entropy(torch.from_numpy(hidden @ W), torch.from_numpy(t), reduction="none")
+    assert rel(res["loss"], ref.numpy()) < 1e-13
+    assert rel(res["lse"], torch.logsumexp(torch.from_numpy(hidden @ W), 1).numpy()) < 1e-14
+
+
+def test_ce_large_logits_no_overflow():
+    hidden = np.array([[1000.0], [-1000.0]])
+    W = np.array([[1.0, 0.5, -2.0]])
+    res = O.lmhead_ce(hidden, W, np.array([0, 2]))
+    # row 0: logits 1000, 500, -2000 -> lse = 1000 + log(1 + e^-500 + ...) = 1000
+    assert abs(res["lse"][0] - 1000.0) < 1e-12 and res["loss"][0] < 1e-12
+    assert abs(res["lse"][1] - 2000.0) < 1e-12 and abs(res["loss"][1]) < 1e-12
+
+
+def test_lse_two_level_equals_definition():
+    rng = np.random.default_rng(11)
+    logits = rng.standard_normal((9, 1000)) * 6
+    direct = np.log(np.sum(np.exp(logits), axis=1))
+    for tile in (1, 7, 128, 256, 999, 1000, 4096):
+        assert rel(O.lse_two_level(logits, tile), direct) < 1e-14
+    # shift invariance: adding c_i to row i adds c_i to the LSE
+    c = rng.standard_normal(9) * 100
+    assert rel(O.lse_two_level(logits + c[:, None], 100) - c, direct) < 1e-12
+
+
+# ---------------------------------------------------------------- RoPE
+
+def test_rope_frequencies_closed_form():
+    f = O.rope_inv_freq(128, 500000.0)
+    for i, v in GOLD["rope_inv_freq_5e5_128"].items():
+        assert abs(f[int(i)] - v) <= 1e-15 * max(v, 1e-300) * 4
+    assert f[0] == 1.0
+
+
+def test_rope_small_closed_form():
+    v = np.array([[1.0, 0.0, 0.0, 1.0]])
+    out = O.rope_apply(v, np.array([3]), n_rope_cols=4, head_dim=4, theta=10000.0)
+    assert rel(out[0], GOLD["rope_hd4_pos3"]) < 1e-15
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(12)
+    hd, nrope, ncols = 16, 48, 64
+    v = rng.standard_normal((10, ncols))
+    pos = rng.integers(0, 4096, 10)
+    r = O.rope_apply(v, pos, nrope, hd, 500000.0)
+    assert np.array_equal(r[:, nrope:], v[:, nrope:])                       # v columns untouched
+    pn = lambda a: a[:, 0:nrope:2] ** 2 + a[:, 1:nrope:2] ** 2
+    assert rel(pn(r), pn(v)) < 1e-14                                          # pair norms kept
+    assert rel(O.rope_apply(r, pos, nrope, hd, 500000.0, inverse=True), v) < 1e-14
+    assert np.array_equal(O.rope_apply(v, np.zeros(10, int), nrope, hd), v)   # pos 0 = identity
+    # relative position: <R(p)q, R(k)k> depends only on p - k, per head
+    q, k = v[0:1], v[1:2]
+    for p1, p2, sh in ((5, 2, 100), (77, 1000, 3)):
+        a = O.rope_apply(q, np.array([p1]), nrope, hd) * O.rope_apply(k, np.array([p2]), nrope, hd)
+        b = O.rope_apply(q, np.array([p1 + sh]), nrope, hd) * O.rope_apply(k, np.array([p2 + sh]), nrope, hd)
+        for h in range(nrope // hd):
+            sl = slice(h * hd, (h + 1) * hd)
+            assert abs(a[0, sl].sum() - b[0, sl].sum()) < 1e-11
+
+
+def test_rope_is_complex_multiplication():
+    # textbook reduction: rotating the pair (e, o) is multiplying e + i o by exp(i angle)
+    rng = np.random.default_rng(13)
+    hd, nrope = 8, 16
+    v = rng.standard_normal((4, 24))
+    pos = np.array([0, 1, 17, 4095])
+    r = O.rope_apply(v, pos, nrope, hd, 500000.0)
+    tv = torch.from_numpy(v[:, :nrope].copy()).reshape(4, nrope // 2, 2)
+    cz = torch.view_as_complex(tv.contiguous())
+    ang = torch.from_numpy(pos.astype(np.float64))[:, None] * torch.from_numpy(
+        np.tile(O.rope_inv_freq(hd, 500000.0), nrope // hd))[None, :]
+    rot = torch.view_as_real(cz * torch.polar(torch.ones_like(ang), ang)).reshape(4, nrope)
+    assert rel(r[:, :nrope], rot.numpy()) < 1e-14
+
+
+# ---------------------------------------------------------------- 8B-shaped block
+
+def rand_8b(M=3, d=8, f=6, hd=4, nq=2, nkv=1, seed=14, wscale=0.3):
+    rng = np.random.default_rng(seed)
+    nqkv = (nq + 2 * nkv) * hd
+    return dict(o=rng.standard_normal((M, d)), z=rng.standard_normal((M, d)),
+                Wo=rng.standard_normal((d, d)) * wscale, W1=rng.standard_normal((d, 2 * f)) * wscale,
+                W2=rng.standard_normal((f, d)) * wscale, gamma2=rng.uniform(0.5, 1.5, d),
+                gamma1=rng.uniform(0.5, 1.5, d), Wqkv=rng.standard_normal((d, nqkv)) * wscale,
+                dqkv=rng.standard_normal((M, nqkv)), dres=rng.standard_normal((M, d))), \
+        (nq + nkv) * hd, hd
+
+
+def _8b(inp, pos, nrope, hd, theta=500000.0):
+    fw = O.block8b_fwd(inp["o"], inp["z"], inp["Wo"], inp["W1"], inp["W2"], inp["gamma2"],
+                       inp["gamma1"], inp["Wqkv"], pos, nrope, hd, theta)
+    return fw
+
+
+def test_block8b_backward_finite_differences():
+    inp, nrope, hd = rand_8b()
+    pos = np.array([0, 3, 11])
+    keys = ("o", "z", "Wo", "W1", "W2", "gamma2", "gamma1", "Wqkv")
+
+    def L(vals):
+        fw = _8b(vals, pos, nrope, hd)
+        return float(np.sum(fw["qkv"] * inp["dqkv"]) + np.sum(fw["out"] * inp["dres"]))
+
+    fw = _8b(inp, pos, nrope, hd)
+    bw = O.block8b_bwd(fw, inp["o"], inp["Wo"], inp["W1"], inp["W2"], inp["gamma2"], inp["gamma1"],
+                       inp["Wqkv"], inp["dqkv"], inp["dres"], pos, nrope, hd)
+    gname = {"o": "do", "z": "dz", "Wo": "dWo", "W1": "dW1", "W2": "dW2", "gamma2": "dgamma2",
+             "gamma1": "dgamma1", "Wqkv": "dWqkv"}
+    for k in keys:
+        fd = np.zeros_like(inp[k])
+        for idx in np.ndindex(inp[k].shape):
+            vals = {kk: np.array(inp[kk], copy=True) for kk in inp}
+            vals[k][idx] += 1e-6
+            lp = L(vals)
+            vals[k][idx] -= 2e-6
+            fd[idx] = (lp - L(vals)) / 2e-6
+        assert rel(bw[gname[k]], fd) < 1e-6, k
+
+
+def test_block8b_matches_torch_autograd():
+    inp, nrope, hd = rand_8b(M=4, d=16, f=8, hd=4, nq=2, nkv=1, seed=15)
+    pos = np.array([0, 1, 2, 3000])
+    t = {k: torch.tensor(v, dtype=torch.float64, requires_grad=k not in ("dqkv", "dres"))
+         for k, v in inp.items()}
+    h = t["o"] @ t["Wo"] + t["z"]
+    h2 = F.rms_norm(h, (16,), t["gamma2"], 1e-6)
+    y = h2 @ t["W1"]
+    out = (F.silu(y[:, 0::2]) * y[:, 1::2]) @ t["W2"] + h
+    q_in = F.rms_norm(out, (16,), t["gamma1"], 1e-6)
+    pre = q_in @ t["Wqkv"]
+    ang = torch.tensor(pos, dtype=torch.float64)[:, None] * torch.tensor(
+        np.tile(O.rope_inv_freq(hd, 500000.0), nrope // hd))[None, :]
+    cz = torch.view_as_complex(pre[:, :nrope].reshape(4, nrope // 2, 2).contiguous())
+    rot = torch.view_as_real(cz * torch.polar(torch.ones_like(ang), ang)).reshape(4, nrope)
+    qkv = torch.cat([rot, pre[:, nrope:]], 1)
+    ((qkv * t["dqkv"]).sum() + (out * t["dres"]).sum()).backward()
+    fw = _8b(inp, pos, nrope, hd)
+    bw = O.block8b_bwd(fw, inp["o"], inp["Wo"], inp["W1"], inp["W2"], inp["gamma2"], inp["gamma1"],
+                       inp["Wqkv"], inp["dqkv"], inp["dres"], pos, nrope, hd)
+    assert rel(fw["qkv"], qkv.detach().numpy()) < 1e-13
+    assert rel(fw["out"], out.detach().numpy()) < 1e-13
+    for k, g in {"o": "do", "z": "dz", "Wo": "dWo", "W1": "dW1", "W2": "dW2", "gamma2": "dgamma2",
+                 "gamma1": "dgamma1", "Wqkv": "dWqkv"}.items():
+        assert rel(bw[g], t[k].grad.numpy()) < 1e-12, k
+
+
+def test_block8b_qkv_statistic_through_rotation():
+    # s' = (1/d) sumcols(dqkv_pre * qkv_pre) = (1/d) sumcols(dqkv * qkv): the
+    # rotation preserves dot products pair by pair.
+    inp, nrope, hd = rand_8b(M=5, d=8, f=6, seed=16)
+    pos = np.array([0, 9, 100, 4095, 7])
+    fw = _8b(inp, pos, nrope, hd)
+    bw = O.block8b_bwd(fw, inp["o"], inp["Wo"], inp["W1"], inp["W2"], inp["gamma2"], inp["gamma1"],
+                       inp["Wqkv"], inp["dqkv"], inp["dres"], pos, nrope, hd)
+    a = np.sum(bw["dqkv_pre"] * fw["qkv_pre"], axis=1)
+    b = np.sum(inp["dqkv"] * fw["qkv"], axis=1)
+    assert rel(a, b) < 1e-13
+    assert rel(bw["s1"], b / 8) < 1e-12
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    """Plants plausible mistakes in the oracle (CPU only) and checks that at
+    least one pin above would catch each one."""
+    inp = rand_block(M=2, d=8, f=8, seed=17)
+    assert fd_block_error(inp) < 1e-6
+    # 1) silu' replaced by sigmoid (dropped term)
+    with monkeypatch.context() as mp:
+        mp.setattr(O, "silu_grad", O.sigmoid)
+        assert fd_block_error(inp) > 1e-3
+    # 2) gate and up swapped in the forward only
+    with monkeypatch.context() as mp:
+        mp.setattr(O, "swiglu", lambda y: O.silu(y[:, 1::2]) * y[:, 0::2])
+        assert fd_block_error(inp) > 1e-3
+    # 3) eps outside the square root
+    with monkeypatch.context() as mp:
+        mp.setattr(O, "rms_factor", lambda h, eps=1e-6: 1.0 / (np.sqrt(np.mean(h * h, 1)) + eps))
+        g = GOLD["block_example"]
+        x = np.array([g["inputs"]["x"]], float)
+        fw = O.mlp_fwd(x, np.array([g["inputs"]["z"]]), np.eye(2), np.eye(2),
+                       np.array([[2.0, -1.0]]), np.array([1.0, 0.5]))
+        assert abs(fw["r"][0] - g["r"]) > 1e-9
