@@ -1,0 +1,529 @@
+// Epilogues for the tcgen05 GEMM, built from the five primitive classes of
+// "Reading notes on CODA", s1 "The Epilogue Concept":
+//   (1) elementwise / pairwise maps        -- in registers, one row per thread
+//   (2) row / column vector loads / stores -- gamma[n], r[m], s[m], targets[m]
+//   (3) tile loads / stores                 -- TMA boxes through swizzled smem
+//   (4) tile reductions                     -- per-row sums (thread-local) and
+//                                              per-column sums (warp transpose)
+//   (5) stateful transforms                 -- running max / sum-exp per row
+//
+// Each epilogue warp owns 32 rows of the 128 x BN accumulator tile (its TMEM
+// lane quarter) and walks the tile in chunks of 32 accumulator columns:
+// tcgen05.ld -> math -> st.shared into a swizzled box -> one TMA store per
+// output. Tile loads for the next chunk are issued before the current chunk
+// is computed (double-buffered staging).
+#pragma once
+#include "gemm.cuh"
+
+namespace coda {
+
+// ------------------------------------------------------------------ helpers
+
+// 32 bf16 values of an n-vector (e.g. gamma) starting at column n (broadcast
+// load: every lane reads the same addresses). Columns >= N read as 0.
+__device__ __forceinline__ void load_nvec32(const __nv_bfloat16* p, int n, int N, float (&o)[32]) {
+  if (n + 32 <= N) {
+    const uint4* q = reinterpret_cast<const uint4*>(p + n);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 u = __ldg(q + k);
+      o[8 * k + 0] = bf16_lo(u.x); o[8 * k + 1] = bf16_hi(u.x);
+      o[8 * k + 2] = bf16_lo(u.y); o[8 * k + 3] = bf16_hi(u.y);
+      o[8 * k + 4] = bf16_lo(u.z); o[8 * k + 5] = bf16_hi(u.z);
+      o[8 * k + 6] = bf16_lo(u.w); o[8 * k + 7] = bf16_hi(u.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = (n + j < N) ? __bfloat162float(p[n + j]) : 0.f;
+  }
+}
+
+// Unpack one 16-byte chunk (8 bf16) from shared memory into o[0..7].
+__device__ __forceinline__ void unpack8(uint4 u, float* o) {
+  o[0] = bf16_lo(u.x); o[1] = bf16_hi(u.x); o[2] = bf16_lo(u.y); o[3] = bf16_hi(u.y);
+  o[4] = bf16_lo(u.z); o[5] = bf16_hi(u.z); o[6] = bf16_lo(u.w); o[7] = bf16_hi(u.w);
+}
+
+// Store 32 fp32 values as bf16 into row `lane` of a 64-byte-row swizzled box.
+__device__ __forceinline__ void stage_bf16x32(uint32_t buf, int lane, const float (&v)[32]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    st_shared_v4(buf + swz<64>(lane, k), pack_bf16(v[8 * k], v[8 * k + 1]),
+                 pack_bf16(v[8 * k + 2], v[8 * k + 3]), pack_bf16(v[8 * k + 4], v[8 * k + 5]),
+                 pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+}
+
+__device__ __forceinline__ void read_bf16x32(uint32_t buf, int lane, float (&v)[32]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) unpack8(ld_shared_v4(buf + swz<64>(lane, k)), &v[8 * k]);
+}
+
+__device__ __forceinline__ float sigmoidf_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+
+// Column sums of a 32 x 32 block held one row per lane: after the exchange,
+// lane j holds the sum over the 32 rows of column j (31 shuffles per lane).
+__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = upper ? v[i] : v[i + s];
+      const float keep = upper ? v[i + s] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
+// ------------------------------------------------------------------ plain
+// C = acc (+ resid), optional per-row sum of squares of the stored value's
+// fp32 pre-image. fp32 output rows are 128 bytes per 32 columns, bf16 64.
+template <bool OUT_F32, bool RESID, bool ROWSQ>
+struct EpiPlain {
+  static_assert(!(OUT_F32 && RESID), "residual is defined for bf16 outputs");
+  static constexpr int kRowB = OUT_F32 ? 128 : 64;
+  static constexpr int kBufB = 32 * kRowB;
+  static constexpr int kSmemPerWarp = 2 * kBufB;
+  struct Params {
+    CUtensorMap tm_c;
+    CUtensorMap tm_r;
+    float* rowsq;  // [tiles_n, M] when ROWSQ
+  };
+  template <int BN>
+  static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
+                                                  int m0, int n0) {
+    if constexpr (RESID) {
+      c.stores_read_done();
+      const int b = c.cnt & 1;
+      c.load(&p.tm_r, b, c.buf + b * kBufB, n0, m0 + 32 * c.q, kBufB);
+    }
+  }
+  template <int BN>
+  static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
+                                              int n0, int nb, uint32_t taddr) {
+    constexpr int NCH = BN / 32;
+    float ss = 0.f;
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int b = c.cnt & 1;
+      const uint32_t buf = c.buf + b * kBufB;
+      c.stores_read_done();
+      if constexpr (RESID) {
+        if (ch + 1 < NCH)
+          c.load(&p.tm_r, b ^ 1, c.buf + (b ^ 1) * kBufB, n0 + (ch + 1) * 32, m0 + 32 * c.q, kBufB);
+      }
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      if constexpr (RESID) {
+        if (!c.wait(b, 10)) return false;
+        float z[32];
+        read_bf16x32(buf, c.lane, z);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += z[j];
+      }
+      if constexpr (ROWSQ) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+      }
+      if constexpr (OUT_F32) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(buf + swz<128>(c.lane, k), __float_as_uint(v[4 * k]),
+                       __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
+                       __float_as_uint(v[4 * k + 3]));
+      } else {
+        stage_bf16x32(buf, c.lane, v);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (c.lane == 0) {
+        tma_store_2d(&p.tm_c, buf, n0 + ch * 32, m0 + 32 * c.q);
+        bulk_commit();
+      }
+      ++c.cnt;
+    }
+    if constexpr (ROWSQ) {
+      const int row = m0 + 32 * c.q + c.lane;
+      if (row < g.M) p.rowsq[(size_t)nb * g.M + row] = ss;
+    }
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------ a1
+// GEMM 1 of GEMM-RMSNorm-GEMM ("Reading notes on CODA", s2; Listing 2
+// "Kernel Example": residual D = acc + C, block sum of squares of the
+// unscaled D, side output D * gamma[n]):
+//   h = acc + z (stored), hg = h * gamma (stored), part[nb, m] = sum_n h^2
+struct EpiResidNormStats {
+  static constexpr int kBufB = 2048;  // 32 rows x 32 bf16
+  static constexpr int kSmemPerWarp = 4 * kBufB;  // H[2] (z in, h out) + G[2]
+  struct Params {
+    CUtensorMap tm_z, tm_h, tm_hg;
+    const __nv_bfloat16* gamma;
+    float* part;  // [tiles_n, M]
+  };
+  template <int BN>
+  static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
+                                                  int m0, int n0) {
+    c.stores_read_done();
+    const int b = c.cnt & 1;
+    c.load(&p.tm_z, b, c.buf + b * kBufB, n0, m0 + 32 * c.q, kBufB);
+  }
+  template <int BN>
+  static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
+                                              int n0, int nb, uint32_t taddr) {
+    constexpr int NCH = BN / 32;
+    float ss = 0.f;
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int b = c.cnt & 1;
+      const uint32_t hbuf = c.buf + b * kBufB;
+      const uint32_t gbuf = c.buf + (2 + b) * kBufB;
+      c.stores_read_done();
+      if (ch + 1 < NCH)
+        c.load(&p.tm_z, b ^ 1, c.buf + (b ^ 1) * kBufB, n0 + (ch + 1) * 32, m0 + 32 * c.q, kBufB);
+      float v[32], gm[32], z[32];
+      tmem_ld32(taddr + ch * 32, v);
+      load_nvec32(p.gamma, n0 + ch * 32, g.N, gm);
+      if (!c.wait(b, 11)) return false;
+      read_bf16x32(hbuf, c.lane, z);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        v[j] += z[j];
+        ss = fmaf(v[j], v[j], ss);
+        gm[j] *= v[j];
+      }
+      stage_bf16x32(hbuf, c.lane, v);
+      stage_bf16x32(gbuf, c.lane, gm);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (c.lane == 0) {
+        tma_store_2d(&p.tm_h, hbuf, n0 + ch * 32, m0 + 32 * c.q);
+        tma_store_2d(&p.tm_hg, gbuf, n0 + ch * 32, m0 + 32 * c.q);
+        bulk_commit();
+      }
+      ++c.cnt;
+    }
+    const int row = m0 + 32 * c.q + c.lane;
+    if (row < g.M) p.part[(size_t)nb * g.M + row] = ss;
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------ a3
+// GEMM 2 with the delayed row scale and the pairwise SwiGLU map ("Reading
+// notes on CODA", s2: y[i,j] = r[i] h3[i,j]; pairwise activations on
+// adjacent accumulator values; pith Fig. 7 caption):
+//   y = r[m] * acc ; a_k = silu(y_2k) * y_2k+1 (stored) ; y optionally stored
+struct EpiRowScaleSwiGLU {
+  static constexpr int kABufB = 1024;  // 32 rows x 16 bf16 (32-byte rows)
+  static constexpr int kYBufB = 2048;  // 32 rows x 32 bf16
+  static constexpr int kSmemPerWarp = 2 * kABufB + 2 * kYBufB;
+  struct Params {
+    CUtensorMap tm_a, tm_y;
+    const float* r;
+    int save_y;
+  };
+  template <int BN>
+  static __device__ __forceinline__ void prefetch(const Params&, EpiCtx&, const GemmArgs&, int, int) {}
+  template <int BN>
+  static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
+                                              int n0, int, uint32_t taddr) {
+    constexpr int NCH = BN / 32;
+    const int row = m0 + 32 * c.q + c.lane;
+    const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int b = c.cnt & 1;
+      const uint32_t abuf = c.buf + b * kABufB;
+      const uint32_t ybuf = c.buf + 2 * kABufB + b * kYBufB;
+      c.stores_read_done();
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      uint32_t ap[8];
+#pragma unroll
+      for (int j = 0; j < 16; j += 2) {
+        const float g0 = rr * v[2 * j], u0 = rr * v[2 * j + 1];
+        const float g1 = rr * v[2 * j + 2], u1 = rr * v[2 * j + 3];
+        const float a0 = g0 * sigmoidf_fast(g0) * u0;
+        const float a1 = g1 * sigmoidf_fast(g1) * u1;
+        ap[j / 2] = pack_bf16(a0, a1);
+        v[2 * j] = g0; v[2 * j + 1] = u0; v[2 * j + 2] = g1; v[2 * j + 3] = u1;
+      }
+      st_shared_v4(abuf + swz<32>(c.lane, 0), ap[0], ap[1], ap[2], ap[3]);
+      st_shared_v4(abuf + swz<32>(c.lane, 1), ap[4], ap[5], ap[6], ap[7]);
+      if (p.save_y) stage_bf16x32(ybuf, c.lane, v);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (c.lane == 0) {
+        tma_store_2d(&p.tm_a, abuf, (n0 + ch * 32) / 2, m0 + 32 * c.q);
+        if (p.save_y) tma_store_2d(&p.tm_y, ybuf, n0 + ch * 32, m0 + 32 * c.q);
+        bulk_commit();
+      }
+      ++c.cnt;
+    }
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------ a5
+// Row scale and pairwise RoPE on adjacent accumulator values (pith Fig. 7
+// caption: RoPE rotates each feature pair and returns two outputs):
+//   v = r[m] * acc ; for columns < n_rope, inside each head_dim-wide head,
+//   (v_2i, v_2i+1) -> (v_2i c - v_2i+1 s, v_2i s + v_2i+1 c),
+//   (c, s) = cos_sin[pos(m), i], pos(m) = m mod seq_len
+struct EpiRope {
+  static constexpr int kBufB = 2048;
+  static constexpr int kSmemPerWarp = 2 * kBufB;
+  struct Params {
+    CUtensorMap tm_out;
+    const float* r;        // nullable: no row scale
+    const float2* cs;      // [seq_len, head_dim/2] (cos, sin)
+    int seq_len, head_dim, n_rope;
+  };
+  template <int BN>
+  static __device__ __forceinline__ void prefetch(const Params&, EpiCtx&, const GemmArgs&, int, int) {}
+  template <int BN>
+  static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
+                                              int n0, int, uint32_t taddr) {
+    constexpr int NCH = BN / 32;
+    const int row = m0 + 32 * c.q + c.lane;
+    const float rr = (p.r == nullptr) ? 1.f : (row < g.M ? __ldg(p.r + row) : 0.f);
+    const int pos = row < g.M ? row % p.seq_len : 0;
+    const float4* csrow = reinterpret_cast<const float4*>(p.cs + (size_t)pos * (p.head_dim / 2));
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int b = c.cnt & 1;
+      const uint32_t buf = c.buf + b * kBufB;
+      c.stores_read_done();
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      const int col0 = n0 + ch * 32;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= rr;
+      if (col0 < p.n_rope) {
+        const int i0 = (col0 % p.head_dim) / 2;  // first pair index in this head
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 t = __ldg(csrow + i0 / 2 + k);  // pairs i0+2k, i0+2k+1
+          const float e0 = v[4 * k], o0 = v[4 * k + 1], e1 = v[4 * k + 2], o1 = v[4 * k + 3];
+          v[4 * k] = e0 * t.x - o0 * t.y;
+          v[4 * k + 1] = e0 * t.y + o0 * t.x;
+          v[4 * k + 2] = e1 * t.z - o1 * t.w;
+          v[4 * k + 3] = e1 * t.w + o1 * t.z;
+        }
+      }
+      stage_bf16x32(buf, c.lane, v);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (c.lane == 0) {
+        tma_store_2d(&p.tm_out, buf, col0, m0 + 32 * c.q);
+        bulk_commit();
+      }
+      ++c.cnt;
+    }
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------ a6
+// LM head + cross-entropy ("Reading notes on CODA", s2 "Cross-entropy loss";
+// thread Pattern 3): logits stay in TMEM/registers. Per row and column tile:
+// running max and sum of exp(l - max) (stateful transform), the target logit
+// picked by an exact index compare (indexed load). Nothing of size M x V is
+// written.
+struct EpiCE {
+  static constexpr int kSmemPerWarp = 0;
+  struct Params {
+    const int* targets;
+    float2* part;    // [tiles_n, M] (max, sumexp)
+    float* tlogit;   // [M]
+  };
+  template <int BN>
+  static __device__ __forceinline__ void prefetch(const Params&, EpiCtx&, const GemmArgs&, int, int) {}
+  template <int BN>
+  static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
+                                              int n0, int nb, uint32_t taddr) {
+    constexpr int NCH = BN / 32;
+    const int row = m0 + 32 * c.q + c.lane;
+    const int tgt = row < g.M ? __ldg(p.targets + row) : -1;
+    float rmax = -INFINITY, rsum = 0.f, tl = 0.f;
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int col0 = n0 + ch * 32;
+      if (col0 >= g.N) break;
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      if (col0 + 32 > g.N) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j >= g.N) v[j] = -INFINITY;
+      }
+      float cmax = v[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
+      const float nmax = fmaxf(rmax, cmax);
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc += __expf(v[j] - nmax);
+      rsum = rsum * __expf(rmax - nmax) + acc;
+      rmax = nmax;
+      const unsigned idx = (unsigned)(tgt - col0);
+      if (idx < 32u) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if ((unsigned)j == idx) tl = v[j];
+      }
+    }
+    if (row < g.M) {
+      p.part[(size_t)nb * g.M + row] = make_float2(rmax, rsum);
+      if (tgt >= n0 && tgt < n0 + BN && tgt < g.N) p.tlogit[row] = tl;
+    }
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------ a7
+// Backward of GEMM 2's epilogue, fused into the GEMM that produces the
+// gradient of its output ("Reading notes on CODA", s3 "Reverse Fusion";
+// pith Fig. 7: the SwiGLU backward maps one incoming gradient to both paired
+// inputs; "Eliminating the RMSNorm backward kernel": the row statistic is
+// accumulated here):
+//   da = acc ; (g, u) = saved y pair ; dg = da u sig(g) (1 + g (1 - sig(g)))
+//   du = da silu(g) ; spart[nb, m] = sum (dg g + du u) ; dyhat = r (dg, du)
+struct EpiSwiGLUBwd {
+  static constexpr int kBufB = 4096;  // 32 rows x 64 bf16 (y in, dyhat out)
+  static constexpr int kSmemPerWarp = 2 * kBufB;
+  struct Params {
+    CUtensorMap tm_y, tm_dy;
+    const float* r;
+    float* spart;  // [tiles_n, M]
+  };
+  template <int BN>
+  static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
+                                                  int m0, int n0) {
+    c.stores_read_done();
+    const int b = c.cnt & 1;
+    c.load(&p.tm_y, b, c.buf + b * kBufB, 2 * n0, m0 + 32 * c.q, kBufB);
+  }
+  template <int BN>
+  static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
+                                              int n0, int nb, uint32_t taddr) {
+    constexpr int NCH = BN / 32;
+    const int row = m0 + 32 * c.q + c.lane;
+    const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
+    float ss = 0.f;
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int b = c.cnt & 1;
+      const uint32_t buf = c.buf + b * kBufB;
+      c.stores_read_done();
+      if (ch + 1 < NCH)
+        c.load(&p.tm_y, b ^ 1, c.buf + (b ^ 1) * kBufB, 2 * (n0 + (ch + 1) * 32), m0 + 32 * c.q, kBufB);
+      float da[32];
+      tmem_ld32(taddr + ch * 32, da);
+      if (!c.wait(b, 12)) return false;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {  // 16-byte chunk k = pairs 4k .. 4k+3
+        const uint32_t addr = buf + swz<128>(c.lane, k);
+        const uint4 u = ld_shared_v4(addr);
+        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+        uint32_t outw[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float gg = bf16_lo(in[t]), uu = bf16_hi(in[t]);
+          const float sg = sigmoidf_fast(gg);
+          const float d = da[4 * k + t];
+          const float dg = d * uu * sg * (1.0f + gg * (1.0f - sg));
+          const float du = d * gg * sg;
+          ss = fmaf(dg, gg, fmaf(du, uu, ss));
+          outw[t] = pack_bf16(rr * dg, rr * du);
+        }
+        st_shared_v4(addr, outw[0], outw[1], outw[2], outw[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (c.lane == 0) {
+        tma_store_2d(&p.tm_dy, buf, 2 * (n0 + ch * 32), m0 + 32 * c.q);
+        bulk_commit();
+      }
+      ++c.cnt;
+    }
+    if (row < g.M) p.spart[(size_t)nb * g.M + row] = ss;
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------ a9
+// RMSNorm backward fused into the GEMM P = dyhat W1^T ("Reading notes on
+// CODA", s3): P = r dh2, so
+//   dh = gamma P - r^2 s h (+ dres) (stored) ; dgamma partial = sum_rows P h
+// The column sums use a warp transpose-reduce; partials are per 32 rows.
+struct EpiNormBwd {
+  static constexpr int kBufB = 2048;
+  static constexpr int kSmemPerWarp = 4 * kBufB;  // H[2] (h in, dh out), R[2] (dres)
+  struct Params {
+    CUtensorMap tm_h, tm_dres, tm_dh;
+    const __nv_bfloat16* gamma;
+    const float* r;
+    const float* s;
+    float* dgpart;  // [ceil(M/32), N]
+    int has_dres;
+  };
+  template <int BN>
+  static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
+                                                  int m0, int n0) {
+    c.stores_read_done();
+    const int b = c.cnt & 1;
+    c.load(&p.tm_h, b, c.buf + b * kBufB, n0, m0 + 32 * c.q, kBufB);
+    if (p.has_dres) c.load(&p.tm_dres, 2 + b, c.buf + (2 + b) * kBufB, n0, m0 + 32 * c.q, kBufB);
+  }
+  template <int BN>
+  static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
+                                              int n0, int, uint32_t taddr) {
+    constexpr int NCH = BN / 32;
+    const int row = m0 + 32 * c.q + c.lane;
+    const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
+    const float ss = row < g.M ? __ldg(p.s + row) : 0.f;
+    const float k2 = rr * rr * ss;
+    const int prow = (m0 >> 5) + c.q;  // partial row (32 rows each)
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int b = c.cnt & 1;
+      const uint32_t hbuf = c.buf + b * kBufB;
+      const uint32_t rbuf = c.buf + (2 + b) * kBufB;
+      c.stores_read_done();
+      if (ch + 1 < NCH) {
+        const int nn = n0 + (ch + 1) * 32;
+        c.load(&p.tm_h, b ^ 1, c.buf + (b ^ 1) * kBufB, nn, m0 + 32 * c.q, kBufB);
+        if (p.has_dres) c.load(&p.tm_dres, 2 + (b ^ 1), c.buf + (2 + (b ^ 1)) * kBufB, nn, m0 + 32 * c.q, kBufB);
+      }
+      float P[32], h[32], gm[32];
+      tmem_ld32(taddr + ch * 32, P);
+      load_nvec32(p.gamma, n0 + ch * 32, g.N, gm);
+      if (!c.wait(b, 13)) return false;
+      read_bf16x32(hbuf, c.lane, h);
+      float dh[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) dh[j] = gm[j] * P[j] - k2 * h[j];
+      if (p.has_dres) {
+        if (!c.wait(2 + b, 14)) return false;
+        float rz[32];
+        read_bf16x32(rbuf, c.lane, rz);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dh[j] += rz[j];
+      }
+      stage_bf16x32(hbuf, c.lane, dh);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (c.lane == 0) {
+        tma_store_2d(&p.tm_dh, hbuf, n0 + ch * 32, m0 + 32 * c.q);
+        bulk_commit();
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) P[j] *= h[j];
+      const float colsum = warp_colsum32(P, c.lane);
+      const int col = n0 + ch * 32 + c.lane;
+      if (col < g.N && m0 + 32 * c.q < g.M) p.dgpart[(size_t)prow * g.N + col] = colsum;
+      ++c.cnt;
+    }
+    return true;
+  }
+};
+
+}  // namespace coda

@@ -1,0 +1,27 @@
+// Plain GEMM instantiations for transposed operands: the data-gradient
+// (A K-major, B K-major) and weight-gradient (A MN-major, B MN-major) shapes.
+#include "core/launch.cuh"
+
+namespace coda {
+
+template <bool AMN, bool BMN, bool F32>
+static cudaError_t plain_t_impl(const PlainArgs& a, const LaunchCtx& lc) {
+  using E = EpiPlain<F32, false, false>;
+  using T = GemmTraits<kTileN, AMN, BMN, E>;
+  typename E::Params p;
+  p.tm_c = a.tmC;
+  p.tm_r = a.tmR;
+  p.rowsq = nullptr;
+  return launch_gemm<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+}
+
+cudaError_t launch_plain_other(const PlainArgs& a, const LaunchCtx& lc) {
+  if (a.resid || a.rowsq) return cudaErrorNotSupported;
+  if (!a.a_mn && !a.b_mn)
+    return a.out_f32 ? plain_t_impl<false, false, true>(a, lc) : plain_t_impl<false, false, false>(a, lc);
+  if (a.a_mn && a.b_mn)
+    return a.out_f32 ? plain_t_impl<true, true, true>(a, lc) : plain_t_impl<true, true, false>(a, lc);
+  return a.out_f32 ? plain_t_impl<true, false, true>(a, lc) : plain_t_impl<true, false, false>(a, lc);
+}
+
+}  // namespace coda

@@ -1,0 +1,101 @@
+// Internal declarations shared by the translation units of libcoda.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include "core/ptx.cuh"
+
+namespace coda {
+
+using bf16 = __nv_bfloat16;
+
+// Launch context passed from the C-ABI layer to the GEMM launchers.
+struct LaunchCtx {
+  cudaStream_t stream;
+  int* err;                        // device error word
+  unsigned long long timeout_ns;   // bound on every wait
+  int num_sms;
+};
+
+// Plain GEMM: C = op(A) op(B) (+ resid), optional per-row sum of squares.
+struct PlainArgs {
+  CUtensorMap tmA, tmB, tmC, tmR;
+  bool a_mn, b_mn, out_f32, resid, rowsq;
+  float* rowsq_part;
+  int M, N, K;
+};
+cudaError_t launch_plain(const PlainArgs& a, const LaunchCtx& lc);
+
+struct ResidNormStatsArgs {
+  CUtensorMap tmA, tmB, tm_z, tm_h, tm_hg;
+  const bf16* gamma;
+  float* part;
+  int M, N, K;
+};
+cudaError_t launch_resid_norm_stats(const ResidNormStatsArgs& a, const LaunchCtx& lc);
+
+struct RowScaleSwiGLUArgs {
+  CUtensorMap tmA, tmB, tm_a, tm_y;
+  const float* r;
+  int save_y;
+  int M, N, K;
+};
+cudaError_t launch_rowscale_swiglu(const RowScaleSwiGLUArgs& a, const LaunchCtx& lc);
+
+struct RopeArgs {
+  CUtensorMap tmA, tmB, tm_out;
+  const float* r;
+  const float2* cs;
+  int seq_len, head_dim, n_rope;
+  int M, N, K;
+};
+cudaError_t launch_rope(const RopeArgs& a, const LaunchCtx& lc);
+
+struct CEArgs {
+  CUtensorMap tmA, tmB;
+  const int* targets;
+  float2* part;
+  float* tlogit;
+  int M, N, K;
+};
+cudaError_t launch_ce(const CEArgs& a, const LaunchCtx& lc);
+
+struct SwiGLUBwdArgs {
+  CUtensorMap tmA, tmB, tm_y, tm_dy;
+  const float* r;
+  float* spart;
+  int M, N, K;
+};
+cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc);
+
+struct NormBwdArgs {
+  CUtensorMap tmA, tmB, tm_h, tm_dres, tm_dh;
+  const bf16* gamma;
+  const float* r;
+  const float* s;
+  float* dgpart;
+  int has_dres;
+  int M, N, K;
+};
+cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc);
+
+// tile width of every GEMM in the library (columns per accumulator tile)
+constexpr int kTileN = 256;
+constexpr int kTileM = 128;
+
+// auxiliary kernels
+cudaError_t launch_row_rms(const float* part, int nparts, int M, float inv_d, float eps, float* r,
+                           cudaStream_t st);
+cudaError_t launch_row_sum_scale(const float* part, int nparts, int M, float scale, float* out,
+                                 cudaStream_t st);
+cudaError_t launch_col_reduce(const float* part, int nparts, int N, float* out, cudaStream_t st);
+cudaError_t launch_ce_combine(const float2* part, int nparts, const float* tlogit, const int* targets,
+                              int M, int V, float* lse, float* loss, int* err, cudaStream_t st);
+cudaError_t launch_rope_table(float2* cs, int seq_len, int head_dim, double theta, cudaStream_t st);
+cudaError_t launch_rope_bwd(const bf16* d, const bf16* q, const float* r, const float2* cs,
+                            int seq_len, int head_dim, int n_rope, bf16* out, float* s, int M, int N,
+                            float inv_d, cudaStream_t st);
+cudaError_t launch_bounded_wait_probe(int* err, unsigned long long timeout_ns, cudaStream_t st);
+
+}  // namespace coda

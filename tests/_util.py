@@ -1,0 +1,32 @@
+"""Shared helpers for the tests: error metrics and tolerances.
+
+Tolerances: bf16 outputs must match the fp64 oracle within a max relative
+error (||gpu - ref||_inf / ||ref||_inf) of 2e-2; fp32 statistics r, s, LSE and
+loss within 1e-3; integer work exactly.
+"""
+import numpy as np
+import torch
+
+TOL_BF16 = 2e-2
+TOL_F32 = 1e-3
+
+
+def to64(t):
+    if isinstance(t, torch.Tensor):
+        return t.detach().to(torch.float64).cpu().numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def maxrel(got, ref) -> float:
+    got = to64(got)
+    ref = to64(ref)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "non-finite values in GPU output"
+    return float(np.max(np.abs(got - ref)) / max(float(np.max(np.abs(ref))), 1e-300))
+
+
+def assert_close(name, got, ref, tol):
+    e = maxrel(got, ref)
+    print(f"{name}: max rel err {e:.3e} (tol {tol:g})")
+    assert e <= tol, f"{name}: max rel err {e:.3e} > {tol:g}"
+    return e

@@ -1,0 +1,102 @@
+"""GPU tests of the plain tcgen05 GEMM through the C ABI (every operand
+majorness, bf16 and fp32 outputs, ragged M/N/K tails, more tiles than SMs),
+the residual / row-statistic epilogue, and the bounded-wait machinery."""
+import numpy as np
+import pytest
+import torch
+
+from tests._util import TOL_BF16, assert_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def coda():
+    import __graft_entry__ as g
+    g.build()
+    import gemm_epilogue_fusion_tcgen05_gb300 as c
+    return c
+
+
+def _rand(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * scale).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("c_fp32", [0, 1])
+@pytest.mark.parametrize("MNK", [(200, 264, 136), (128, 256, 64), (8, 8, 8), (16, 8, 24)])
+def test_gemm_majorness_ragged(coda, transA, transB, c_fp32, MNK):
+    M, N, K = MNK
+    A = _rand((K, M) if transA else (M, K), 1)
+    B = _rand((N, K) if transB else (K, N), 2)
+    Ad = A.cuda()
+    Bd = B.cuda()
+    C = torch.full((M, N), float("nan"), dtype=torch.float32 if c_fp32 else torch.bfloat16,
+                   device="cuda")
+    coda.coda_gemm(Ad, Bd, C, transA=bool(transA), transB=bool(transB))
+    torch.cuda.synchronize()
+    a = to64(A).T if transA else to64(A)
+    b = to64(B).T if transB else to64(B)
+    ref = a @ b
+    tol = 1e-5 if c_fp32 else TOL_BF16
+    assert_close(f"gemm tA={transA} tB={transB} f32={c_fp32} {MNK}", C, ref, tol)
+    assert coda.get_device_error() == 0
+
+
+def test_gemm_single_row(coda):
+    A, B = _rand((1, 40), 11), _rand((40, 24), 12)
+    C = torch.empty((1, 24), dtype=torch.float32, device="cuda")
+    coda.coda_gemm(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    assert_close("gemm M=1", C, to64(A) @ to64(B), 1e-5)
+
+
+@pytest.mark.parametrize("transA,transB", [(0, 0), (1, 0), (0, 1)])
+def test_gemm_many_tiles_per_cta(coda, transA, transB):
+    # 32 x 16 = 512 tiles > SM count: each CTA walks several tiles and both
+    # TMEM accumulator buffers; K = 320 is 5 k-blocks (ring wraps several times)
+    M, N, K = 4096, 4096, 320
+    A = _rand((K, M) if transA else (M, K), 3)
+    B = _rand((N, K) if transB else (K, N), 4)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    coda.coda_gemm(A.cuda(), B.cuda(), C, transA=bool(transA), transB=bool(transB))
+    torch.cuda.synchronize()
+    a = to64(A).T if transA else to64(A)
+    b = to64(B).T if transB else to64(B)
+    assert_close("gemm 4096^2 x 320", C, a @ b, 1e-5)
+
+
+def test_gemm_strided_operands(coda):
+    # leading dimensions larger than the logical width (views into wider buffers)
+    M, N, K = 136, 72, 96
+    Abig = _rand((M, K + 40), 5)
+    Bbig = _rand((K, N + 24), 6)
+    Cbig = torch.zeros((M, N + 8), dtype=torch.bfloat16, device="cuda")
+    Ad, Bd = Abig.cuda(), Bbig.cuda()
+    coda.coda_gemm(Ad[:, :K], Bd[:, :N], Cbig[:, :N])
+    torch.cuda.synchronize()
+    assert_close("gemm strided", Cbig[:, :N], to64(Abig[:, :K]) @ to64(Bbig[:, :N]), TOL_BF16)
+    assert torch.all(Cbig[:, N:] == 0), "wrote outside the logical columns"
+
+
+@pytest.mark.parametrize("MNK", [(200, 520, 72), (64, 256, 256)])
+def test_gemm_resid_rowsq(coda, MNK):
+    M, N, K = MNK
+    A, B, R = _rand((M, K), 7), _rand((K, N), 8, 0.1), _rand((M, N), 9)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    part = torch.empty((coda.col_tiles(N), M), dtype=torch.float32, device="cuda")
+    coda.coda_gemm(A.cuda(), B.cuda(), C, resid=R.cuda(), rowsq_part=part)
+    torch.cuda.synchronize()
+    ref = to64(A) @ to64(B) + to64(R)
+    assert_close("gemm+resid", C, ref, TOL_BF16)
+    assert_close("row sum of squares", part.sum(0), np.sum(ref * ref, axis=1), 1e-3)
+
+
+def test_bounded_wait_gives_up_without_fault(coda):
+    st = coda.coda_selftest_bounded_wait(20)
+    assert st == coda.CODA_ERR_TIMEOUT
+    # the context is still usable and the error word was cleared
+    assert coda.get_device_error() == 0
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum()) == 4.0
