@@ -1,0 +1,505 @@
+"""Benchmark of the CODA GEMM-plus-epilogue hot path on one GB300 (or N
+replicas, one per GPU, under torchrun).
+
+One step = one pass over every kernel of the hot path:
+  * Llama-3-1B-shaped MLP block forward, M=8192, d=2048, f=8192
+      (residual+RMSNorm-weight+row-stats GEMM, r, delayed-r SwiGLU GEMM,
+       down projection)
+  * LM head + cross-entropy, M=8192, d=2048, V=128256 (logits never written)
+  * the block's reverse-fused backward (SwiGLU-bwd GEMM + s partials, s,
+    RMSNorm-bwd GEMM + dgamma partials, dgamma, dW2, dW1, dW0, dx)
+  * Llama-3-8B-shaped non-attention forward + backward, M=16384, d=4096,
+    f=14336, QKV 6144 with RoPE (theta 5e5, positions 0..4095 per sequence)
+The metric is the GEMM work of the step (2*M*N*K per GEMM) per second; the
+LM head is also reported as tokens/s. Inputs are synthetic (seeded, the
+workloads' distributions), resident in HBM before the timed region; L2 is
+flushed (a 512 MiB write) before every timed step, outside the step's events.
+
+--impl reference times the CPU oracle (fp64 numpy) on a bounded row sample of
+the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "fused GEMM+epilogue TFLOP/s (% BF16 peak); LM-head+CE tokens/s"
+UNIT = "TFLOP/s"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class Clocks:
+    """Samples nvidia-smi every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "gemm_epilogue_fusion_tcgen05_gb300", "csrc")
+    for base, _, files in sorted(os.walk(d)):
+        for f in sorted(files):
+            if f.endswith((".cu", ".cuh", ".h")):
+                h.update(open(os.path.join(base, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ the step
+
+class Step:
+    """Buffers and the list of C-ABI calls of one step. Each call is wrapped
+    in CUDA events on the launching (current) stream."""
+
+    def __init__(self, dev, with_8b=True):
+        import gemm_epilogue_fusion_tcgen05_gb300 as C
+        from gemm_epilogue_fusion_tcgen05_gb300 import blocks
+        from coda_inputs import WORKLOADS, mlp_block_inputs, lmhead_inputs, block8b_inputs
+        self.C = C
+        self.dev = dev
+        bf, f32 = torch.bfloat16, torch.float32
+        e = lambda s, dt: torch.empty(s, dtype=dt, device=dev)
+        # ---- Llama-3-1B-shaped block (forward state kept for the backward)
+        s1 = WORKLOADS["llama1b_mlp_bwd"]
+        self.s1 = s1
+        M, d, f = s1.M, s1.d, s1.f
+        self.i1 = mlp_block_inputs(s1, device=dev)
+        self.b1 = {"h": e((M, d), bf), "hg": e((M, d), bf), "part": e((C.col_tiles(d), M), f32),
+                   "r": e((M,), f32), "a": e((M, f), bf), "y": e((M, 2 * f), bf),
+                   "out": e((M, d), bf), "dyhat": e((M, 2 * f), bf),
+                   "spart": e((C.col_tiles(f), M), f32), "s": e((M,), f32), "dh": e((M, d), bf),
+                   "dgpart": e((C.row_tiles32(M), d), f32), "dgamma": e((d,), f32),
+                   "dW0": e((d, d), f32), "dW1": e((d, 2 * f), f32), "dW2": e((f, d), f32),
+                   "dx": e((M, d), bf)}
+        # ---- LM head
+        s2 = WORKLOADS["lmhead_ce"]
+        self.s2 = s2
+        self.i2 = lmhead_inputs(s2, device=dev)
+        self.ws2 = torch.empty(C.coda_lmhead_ce_workspace_size(s2.M, s2.V), dtype=torch.uint8,
+                               device=dev)
+        self.o2 = {"lse": e((s2.M,), f32), "loss": e((s2.M,), f32)}
+        # ---- Llama-3-8B-shaped block
+        self.with_8b = with_8b
+        if with_8b:
+            s4 = WORKLOADS["llama8b_block"]
+            self.s4 = s4
+            self.i4 = block8b_inputs(s4, device=dev)
+            self.cs = blocks.rope_table(s4.seq_len, s4.head_dim, s4.theta, dev)
+            M4, d4, f4, n4 = s4.M, s4.d, s4.f, s4.n_qkv
+            self.b4 = {"h": e((M4, d4), bf), "hg": e((M4, d4), bf),
+                       "part": e((C.col_tiles(d4), M4), f32), "r": e((M4,), f32),
+                       "a": e((M4, f4), bf), "y": e((M4, 2 * f4), bf), "out": e((M4, d4), bf),
+                       "outg": e((M4, d4), bf), "part1": e((C.col_tiles(d4), M4), f32),
+                       "r1": e((M4,), f32), "qkv": e((M4, n4), bf), "dqh": e((M4, n4), bf),
+                       "s1": e((M4,), f32), "dout": e((M4, d4), bf),
+                       "dgp1": e((C.row_tiles32(M4), d4), f32), "dgamma1": e((d4,), f32),
+                       "dWqkv": e((d4, n4), f32), "dyhat": e((M4, 2 * f4), bf),
+                       "spart": e((C.col_tiles(f4), M4), f32), "s": e((M4,), f32),
+                       "dW2": e((f4, d4), f32), "dh": e((M4, d4), bf),
+                       "dgp2": e((C.row_tiles32(M4), d4), f32), "dgamma2": e((d4,), f32),
+                       "dW1": e((d4, 2 * f4), f32), "dWo": e((d4, d4), f32), "do": e((M4, d4), bf)}
+        self.calls = self._build_calls()
+        self.launches_per_step = sum(c[3] for c in self.calls)
+        self.flops = sum(c[1] for c in self.calls)
+
+    def _build_calls(self):
+        C = self.C
+        i1, b1 = self.i1, self.b1
+        M, d, f = self.s1.M, self.s1.d, self.s1.f
+        calls = []  # (name, flops, fn, launches)
+        add = lambda n, fl, fn, k=1: calls.append((n, float(fl), fn, k))
+        add("1b.gemm_resid_norm_stats", 2 * M * d * d,
+            lambda: C.coda_gemm_resid_norm_stats(i1["x"], i1["W0"], i1["z"], i1["gamma"], b1["h"],
+                                                 b1["hg"], b1["part"]))
+        add("1b.row_rms", 0, lambda: C.coda_row_rms(b1["part"], b1["r"], d, 1e-6))
+        add("1b.gemm_rowscale_swiglu", 2 * M * d * 2 * f,
+            lambda: C.coda_gemm_rowscale_swiglu(b1["hg"], i1["W1"], b1["r"], b1["a"], b1["y"]))
+        add("1b.gemm_down", 2 * M * f * d, lambda: C.coda_gemm(b1["a"], i1["W2"], b1["out"]))
+        s2, i2 = self.s2, self.i2
+        add("lmhead_ce", 2 * s2.M * s2.d * s2.V,
+            lambda: C.coda_lmhead_ce(i2["hidden"], i2["W"], i2["targets"], self.o2["lse"],
+                                     self.o2["loss"], self.ws2), 2)
+        add("1b.gemm_rowscale_swiglu_bwd", 2 * M * d * f,
+            lambda: C.coda_gemm_rowscale_swiglu_bwd(i1["dout"], i1["W2"], b1["y"], b1["r"],
+                                                    b1["dyhat"], b1["spart"]))
+        add("1b.row_rms_bwd", 0, lambda: C.coda_row_rms_bwd(b1["spart"], b1["s"], d))
+        add("1b.gemm_resid_norm_stats_bwd", 2 * M * 2 * f * d,
+            lambda: C.coda_gemm_resid_norm_stats_bwd(b1["dyhat"], i1["W1"], b1["h"], i1["gamma"],
+                                                     b1["r"], b1["s"], b1["dh"], b1["dgpart"]))
+        add("1b.col_reduce", 0, lambda: C.coda_col_reduce(b1["dgpart"], b1["dgamma"]))
+        add("1b.wgrad_W2", 2 * f * d * M, lambda: C.coda_gemm(b1["a"], i1["dout"], b1["dW2"], transA=True))
+        add("1b.wgrad_W1", 2 * d * 2 * f * M, lambda: C.coda_gemm(b1["hg"], b1["dyhat"], b1["dW1"], transA=True))
+        add("1b.wgrad_W0", 2 * d * d * M, lambda: C.coda_gemm(i1["x"], b1["dh"], b1["dW0"], transA=True))
+        add("1b.dgrad_x", 2 * M * d * d, lambda: C.coda_gemm(b1["dh"], i1["W0"], b1["dx"], transB=True))
+        if self.with_8b:
+            s4, i4, b4, cs = self.s4, self.i4, self.b4, self.cs
+            M4, d4, f4, n4 = s4.M, s4.d, s4.f, s4.n_qkv
+            sl, hd, nr = s4.seq_len, s4.head_dim, s4.n_rope_cols
+            add("8b.gemm_resid_norm_stats(Wo)", 2 * M4 * d4 * d4,
+                lambda: C.coda_gemm_resid_norm_stats(i4["o"], i4["Wo"], i4["z"], i4["gamma2"],
+                                                     b4["h"], b4["hg"], b4["part"]))
+            add("8b.row_rms", 0, lambda: C.coda_row_rms(b4["part"], b4["r"], d4, 1e-6))
+            add("8b.gemm_rowscale_swiglu", 2 * M4 * d4 * 2 * f4,
+                lambda: C.coda_gemm_rowscale_swiglu(b4["hg"], i4["W1"], b4["r"], b4["a"], b4["y"]))
+            add("8b.gemm_resid_norm_stats(W2)", 2 * M4 * f4 * d4,
+                lambda: C.coda_gemm_resid_norm_stats(b4["a"], i4["W2"], b4["h"], i4["gamma1"],
+                                                     b4["out"], b4["outg"], b4["part1"]))
+            add("8b.row_rms1", 0, lambda: C.coda_row_rms(b4["part1"], b4["r1"], d4, 1e-6))
+            add("8b.gemm_rope", 2 * M4 * d4 * n4,
+                lambda: C.coda_gemm_rope(b4["outg"], i4["Wqkv"], b4["r1"], cs, sl, hd, nr, b4["qkv"]))
+            add("8b.rope_bwd", 0,
+                lambda: C.coda_gemm_rope_bwd(i4["dqkv"], b4["qkv"], b4["r1"], cs, sl, hd, nr,
+                                             b4["dqh"], b4["s1"], d4))
+            add("8b.gemm_resid_norm_stats_bwd(Wqkv)", 2 * M4 * n4 * d4,
+                lambda: C.coda_gemm_resid_norm_stats_bwd(b4["dqh"], i4["Wqkv"], b4["out"],
+                                                         i4["gamma1"], b4["r1"], b4["s1"],
+                                                         b4["dout"], b4["dgp1"], dresid=i4["dres"]))
+            add("8b.col_reduce1", 0, lambda: C.coda_col_reduce(b4["dgp1"], b4["dgamma1"]))
+            add("8b.wgrad_Wqkv", 2 * d4 * n4 * M4,
+                lambda: C.coda_gemm(b4["outg"], b4["dqh"], b4["dWqkv"], transA=True))
+            add("8b.gemm_rowscale_swiglu_bwd", 2 * M4 * d4 * f4,
+                lambda: C.coda_gemm_rowscale_swiglu_bwd(b4["dout"], i4["W2"], b4["y"], b4["r"],
+                                                        b4["dyhat"], b4["spart"]))
+            add("8b.row_rms_bwd", 0, lambda: C.coda_row_rms_bwd(b4["spart"], b4["s"], d4))
+            add("8b.wgrad_W2", 2 * f4 * d4 * M4,
+                lambda: C.coda_gemm(b4["a"], b4["dout"], b4["dW2"], transA=True))
+            add("8b.gemm_resid_norm_stats_bwd(W1)", 2 * M4 * 2 * f4 * d4,
+                lambda: C.coda_gemm_resid_norm_stats_bwd(b4["dyhat"], i4["W1"], b4["h"],
+                                                         i4["gamma2"], b4["r"], b4["s"], b4["dh"],
+                                                         b4["dgp2"], dresid=b4["dout"]))
+            add("8b.col_reduce2", 0, lambda: C.coda_col_reduce(b4["dgp2"], b4["dgamma2"]))
+            add("8b.wgrad_W1", 2 * d4 * 2 * f4 * M4,
+                lambda: C.coda_gemm(b4["hg"], b4["dyhat"], b4["dW1"], transA=True))
+            add("8b.wgrad_Wo", 2 * d4 * d4 * M4, lambda: C.coda_gemm(i4["o"], b4["dh"], b4["dWo"], transA=True))
+            add("8b.dgrad_o", 2 * M4 * d4 * d4, lambda: C.coda_gemm(b4["dh"], i4["Wo"], b4["do"], transB=True))
+        return calls
+
+    def run(self, events=None):
+        for k, (name, fl, fn, nl) in enumerate(self.calls):
+            if events is not None:
+                events[k][0].record()
+            fn()
+            if events is not None:
+                events[k][1].record()
+
+    # per-step inputs and results for the end-to-end measurement
+    def host_io(self):
+        ins = [self.i1["x"], self.i1["z"], self.i1["dout"], self.i2["hidden"], self.i2["targets"]]
+        if self.with_8b:
+            ins += [self.i4["o"], self.i4["z"], self.i4["dqkv"], self.i4["dres"]]
+        outs = [self.o2["loss"], self.o2["lse"], self.b1["dgamma"]]
+        return ins, outs
+
+
+def run_coda(args):
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__ as g
+    g.build()
+    import gemm_epilogue_fusion_tcgen05_gb300 as C
+
+    step = Step(dev, with_8b=not args.no_8b)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    st = C.get_device_error()
+    if st != 0:
+        raise SystemExit(f"device error after warm-up: {st}")
+
+    n = len(step.calls)
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in range(n)] for _ in range(args.steps)]
+    step_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+               for _ in range(args.steps)]
+    clocks = Clocks(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                    if False else local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        step_ev[i][0].record(stream)
+        step.run(evs[i])
+        step_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    st = C.get_device_error()
+    if st != 0:
+        raise SystemExit(f"device error in timed region: {st}")
+
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    ms = sum(step_ms) / len(step_ms)
+    per_call = [0.0] * n
+    for i in range(args.steps):
+        for k in range(n):
+            per_call[k] += evs[i][k][0].elapsed_time(evs[i][k][1])
+    per_call = [t / args.steps for t in per_call]
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = step.flops * ws / (ms * 1e-3) / 1e12
+
+    # end-to-end through the public API with host buffers: copy this step's
+    # inputs host -> device from pinned memory, run, read the results back
+    ins, outs = step.host_io()
+    h_ins = [t.cpu().pin_memory() for t in ins]
+    h_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in h_ins)
+    d2h = sum(t.numel() * t.element_size() for t in h_outs)
+    e2e_steps = max(2, min(args.steps, 5))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for i in range(e2e_steps):
+        flush.fill_(float(i))
+        e0.record(stream)
+        for hsrc, ddst in zip(h_ins, ins):
+            ddst.copy_(hsrc, non_blocking=True)
+        step.run()
+        for dsrc, hdst in zip(outs, h_outs):
+            hdst.copy_(dsrc, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= e2e_steps
+    e2e_value = step.flops * ws / (e2e_ms * 1e-3) / 1e12
+
+    peaks, src = _peaks()
+    k_dom = max(range(n), key=lambda k: per_call[k])
+    name, fl, _, nl = step.calls[k_dom]
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    achieved = fl / (per_call[k_dom] * 1e-3) / 1e12 if per_call[k_dom] > 0 else None
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        tj = json.load(open(tp))
+        ent = tj.get("kernels", {}).get(name)
+        if ent and tj.get("kernel_hash") == _kernel_hash():
+            traffic = ent.get("dram_bytes_per_launch")
+    lm = [k for k in range(n) if step.calls[k][0] == "lmhead_ce"][0]
+    lm_tok_s = step.s2.M / (per_call[lm] * 1e-3)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; workloads' shapes and distributions; drawn on the GPU)",
+        "config": {"workload": "llama1b_mlp_fwd+lmhead_ce+llama1b_mlp_bwd" +
+                               ("+llama8b_block_fwd_bwd" if step.with_8b else ""),
+                   "tokens": step.s1.M, "d": step.s1.d, "f": step.s1.f, "vocab": step.s2.V,
+                   "tokens_8b": step.s4.M if step.with_8b else 0,
+                   "gflop_per_step": round(step.flops / 1e9, 1),
+                   "l2": "flushed before each step (512 MiB write, outside the step events)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "pct_bf16_peak": round(100 * value / ws / peak, 2),
+        "lmhead_ce_tokens_per_s": round(lm_tok_s, 1),
+        "gpu_launches": step.launches_per_step * args.steps,
+        "wall_s_timed_region": round(wall, 4),
+        "roofline": {"kernel": name, "bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{src} bf16_tflops_sustained (timed inside a long step)",
+                     "flops_per_launch": fl, "ms_per_launch": round(per_call[k_dom], 4),
+                     "traffic": traffic},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clk,
+        "parts_ms": {step.calls[k][0]: round(per_call[k], 4) for k in range(n)},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def _oracle_sample(rows1, rows_ce, rows8):
+    """The CPU oracle, as it stands, on the first rows of each part of the
+    step. Returns (flops, seconds); flops counted like the GPU metric."""
+    import numpy as np
+    from coda_inputs import WORKLOADS, BlockShape, LMHeadShape, Block8BShape, \
+        mlp_block_inputs, lmhead_inputs, block8b_inputs, positions
+    from oracle import coda_oracle as O
+    s1 = WORKLOADS["llama1b_mlp_bwd"]
+    s2 = WORKLOADS["lmhead_ce"]
+    s4 = WORKLOADS["llama8b_block"]
+    # draw the sample directly at its row count (same recipe, fewer rows)
+    i1 = mlp_block_inputs(BlockShape("s", rows1, s1.d, s1.f, s1.seed))
+    i2 = lmhead_inputs(LMHeadShape("s", rows_ce, s2.d, s2.V, s2.seed))
+    i4 = block8b_inputs(Block8BShape("s", rows8, s4.d, s4.f, s4.seq_len, s4.head_dim,
+                                     s4.n_q_heads, s4.n_kv_heads, s4.theta, s4.seed))
+    n1 = {k: O.to64(v) for k, v in i1.items()}
+    n2 = {k: O.to64(v) for k, v in i2.items()}
+    n4 = {k: O.to64(v) for k, v in i4.items()}
+    pos = positions(rows8, s4.seq_len).numpy()
+    t0 = time.perf_counter()
+    fw = O.mlp_fwd(n1["x"], n1["z"], n1["W0"], n1["W1"], n1["W2"], n1["gamma"])
+    O.mlp_bwd(fw, n1["x"], n1["W0"], n1["W1"], n1["W2"], n1["gamma"], n1["dout"])
+    O.lmhead_ce(n2["hidden"], n2["W"], i2["targets"].numpy())
+    f4 = O.block8b_fwd(n4["o"], n4["z"], n4["Wo"], n4["W1"], n4["W2"], n4["gamma2"], n4["gamma1"],
+                       n4["Wqkv"], pos, s4.n_rope_cols, s4.head_dim, s4.theta)
+    O.block8b_bwd(f4, n4["o"], n4["Wo"], n4["W1"], n4["W2"], n4["gamma2"], n4["gamma1"],
+                  n4["Wqkv"], n4["dqkv"], n4["dres"], pos, s4.n_rope_cols, s4.head_dim, s4.theta)
+    dt = time.perf_counter() - t0
+    d, f = s1.d, s1.f
+    fl1 = rows1 * 3 * 2 * (d * d + d * 2 * f + f * d)
+    fl2 = rows_ce * 2 * s2.d * s2.V
+    d4, f4_, n4q = s4.d, s4.f, s4.n_qkv
+    fl4 = rows8 * 3 * 2 * (d4 * d4 + d4 * 2 * f4_ + f4_ * d4 + d4 * n4q)
+    return float(fl1 + fl2 + fl4), dt
+
+
+def cpu_baseline(seconds_target=15.0):
+    rows = (512, 64, 64)
+    fl, dt = _oracle_sample(*rows)
+    scale = max(1.0, min(8.0, seconds_target / max(dt, 1e-3)))
+    if scale > 1.5:
+        rows = tuple(max(8, int(r * scale) // 8 * 8) for r in rows)
+        fl, dt = _oracle_sample(*rows)
+    return {"value": round(fl / dt / 1e12, 5), "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"fp64 numpy oracle on {rows[0]} rows of the 1B block fwd+bwd, {rows[1]} rows "
+                      f"of the LM head, {rows[2]} rows of the 8B block fwd+bwd ({dt:.1f} s, "
+                      f"{fl / 1e12:.2f} TFLOP)"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    rows = (256, 32, 32)
+    for _ in range(args.warmup):
+        _oracle_sample(*rows)
+    fl_tot, dt_tot = 0.0, 0.0
+    for _ in range(args.steps):
+        fl, dt = _oracle_sample(*rows)
+        fl_tot += fl
+        dt_tot += dt
+    v = fl_tot / dt_tot / 1e12
+    line = {"metric": METRIC, "value": round(v, 5), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * dt_tot / args.steps, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
+            "data": "synthetic (seeded; CPU draws)",
+            "config": {"workload": "llama1b_mlp_fwd+lmhead_ce+llama1b_mlp_bwd+llama8b_block_fwd_bwd",
+                       "sample_rows": {"1b": rows[0], "lmhead": rows[1], "8b": rows[2]}},
+            "cpu_baseline": {"value": round(v, 5), "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"fp64 numpy oracle, {rows[0]}/{rows[1]}/{rows[2]} rows "
+                                       "of the 1B block / LM head / 8B block per step"},
+            "e2e": {"value": round(v, 5), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["coda", "reference"], default="coda")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-8b", action="store_true", help="leave the 8B-shaped block out of the step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("note: at least 3 warm-up steps are required; using 3", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_coda(args)
+
+
+if __name__ == "__main__":
+    main()

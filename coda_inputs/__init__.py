@@ -4,9 +4,11 @@ This module is shared by the CPU oracle's tests, the GPU parity tests and the
 benchmark. It only draws random numbers and names shapes: it holds none of the
 method's arithmetic (no GEMM, normalisation, activation or loss).
 
-All tensors are drawn on the CPU from one ``torch.Generator`` per workload, in a
-fixed order, in fp32, then rounded to bf16 (round-to-nearest-even, torch's own
-conversion). The value distributions follow the workload definitions:
+All tensors are drawn from one ``torch.Generator`` per workload, in a fixed
+order, in fp32, then rounded to bf16 (round-to-nearest-even, torch's own
+conversion). Parity tests draw on the CPU (``device="cpu"``, the default);
+the benchmark may draw the same distributions on the GPU's generator to start
+faster (different numbers, same recipe). The value distributions follow the workload definitions:
 activations and upstream gradients ~N(0,1), weights ~N(0, 0.02^2), RMSNorm
 weights ~U[0.5, 1.5], LM-head targets ~U{0, V-1} as int32.
 """
@@ -85,23 +87,27 @@ WORKLOADS = {
 }
 
 
+def _gen(seed: int, device) -> torch.Generator:
+    return torch.Generator(device=device).manual_seed(seed)
+
+
 def _normal(g: torch.Generator, shape, std: float = 1.0) -> torch.Tensor:
-    t = torch.randn(*shape, generator=g, dtype=torch.float32)
+    t = torch.randn(*shape, generator=g, dtype=torch.float32, device=g.device)
     if std != 1.0:
         t.mul_(std)
     return t.to(torch.bfloat16)
 
 
 def _uniform(g: torch.Generator, shape, lo: float, hi: float) -> torch.Tensor:
-    t = torch.rand(*shape, generator=g, dtype=torch.float32)
+    t = torch.rand(*shape, generator=g, dtype=torch.float32, device=g.device)
     return (t * (hi - lo) + lo).to(torch.bfloat16)
 
 
-def mlp_block_inputs(shape: BlockShape, with_grad: bool = True) -> Dict[str, torch.Tensor]:
+def mlp_block_inputs(shape: BlockShape, with_grad: bool = True, device="cpu") -> Dict[str, torch.Tensor]:
     """x, z [M,d]; W0 [d,d]; W1 [d,2f] (column 2k = gate k, 2k+1 = up k);
     W2 [f,d]; gamma [d]; dout [M,d] (upstream gradient of the block output).
     All bf16 on the CPU, drawn in exactly this order."""
-    g = torch.Generator().manual_seed(shape.seed)
+    g = _gen(shape.seed, device)
     M, d, f = shape.M, shape.d, shape.f
     out = {
         "x": _normal(g, (M, d)),
@@ -116,22 +122,23 @@ def mlp_block_inputs(shape: BlockShape, with_grad: bool = True) -> Dict[str, tor
     return out
 
 
-def lmhead_inputs(shape: LMHeadShape) -> Dict[str, torch.Tensor]:
+def lmhead_inputs(shape: LMHeadShape, device="cpu") -> Dict[str, torch.Tensor]:
     """hidden [M,d] bf16 ~N(0,1); W [d,V] bf16 ~N(0,0.02^2); targets int32 [M]."""
-    g = torch.Generator().manual_seed(shape.seed)
+    g = _gen(shape.seed, device)
     hidden = _normal(g, (shape.M, shape.d))
     W = _normal(g, (shape.d, shape.V), 0.02)
-    targets = torch.randint(0, shape.V, (shape.M,), generator=g, dtype=torch.int64).to(torch.int32)
+    targets = torch.randint(0, shape.V, (shape.M,), generator=g, dtype=torch.int64,
+                            device=g.device).to(torch.int32)
     return {"hidden": hidden, "W": W, "targets": targets}
 
 
-def block8b_inputs(shape: Block8BShape, with_grad: bool = True) -> Dict[str, torch.Tensor]:
+def block8b_inputs(shape: Block8BShape, with_grad: bool = True, device="cpu") -> Dict[str, torch.Tensor]:
     """o (attention-output stand-in) and z (residual stream) [M,d]; Wo [d,d];
     W1 [d,2f] gate/up interleaved; W2 [f,d]; gamma2 (pre-MLP norm) and gamma1
     (next pre-attention norm) [d]; Wqkv [d, n_qkv]; upstream gradients dqkv
     [M, n_qkv] (of the rotated q,k and of v) and dres [M,d] (of the residual
     stream leaving the block)."""
-    g = torch.Generator().manual_seed(shape.seed)
+    g = _gen(shape.seed, device)
     M, d, f, n = shape.M, shape.d, shape.f, shape.n_qkv
     out = {
         "o": _normal(g, (M, d)),

@@ -196,7 +196,7 @@ def mlp_bwd(fwd: Dict[str, np.ndarray], x, W0, W1, W2, gamma, dout) -> Dict[str,
 
 
 def mlp_bwd_reparam(fwd: Dict[str, np.ndarray], x, W0, W1, W2, gamma, dout,
-                    store_bf16: bool = False) -> Dict[str, np.ndarray]:
+                    store_bf16: bool = False, stat_only: bool = False) -> Dict[str, np.ndarray]:
     """The pages' reverse-fused backward [notes s3 "Reverse Fusion" and
     "Eliminating the RMSNorm backward kernel"], on the tensors saved by
     ``mlp_fwd_reparam`` (h, hg, r, y, a):
@@ -208,7 +208,7 @@ def mlp_bwd_reparam(fwd: Dict[str, np.ndarray], x, W0, W1, W2, gamma, dout,
         GEMM (dyhat W1^T) epilogue: P = r dh2;  dh = gamma * P - r^2 s h ;
             dgamma = sum_rows P * h
         dW1 = hg^T dyhat ; dW2 = a^T dout ; dx = dh W0^T ; dW0 = x^T dh
-    """
+    ``stat_only`` stops after s (and dy, dyhat)."""
     st = _store(store_bf16)
     x, W0, W1, W2, gamma, dout = (np.asarray(t, dtype=f64) for t in (x, W0, W1, W2, gamma, dout))
     h, hg, r, y, a = (fwd[k] for k in ("h", "hg", "r", "y", "a"))
@@ -221,6 +221,8 @@ def mlp_bwd_reparam(fwd: Dict[str, np.ndarray], x, W0, W1, W2, gamma, dout,
     dy[:, 1::2] = da * silu(g)
     s = np.sum(dy * y, axis=1) / d
     dyhat = st(r[:, None] * dy)
+    if stat_only:
+        return {"dy": dy, "dyhat": dyhat, "s": s}
     P = dyhat @ W1.T
     dh = st(gamma[None, :] * P - (r * r * s)[:, None] * h)
     dgamma = np.sum(P * h, axis=0)
