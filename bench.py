@@ -248,8 +248,19 @@ class Step:
             add("8b.dgrad_o", 2 * M4 * d4 * d4, lambda: C.coda_gemm(b4["dh"], i4["Wo"], b4["do"], transB=True))
         return calls
 
-    def run(self, events=None):
-        for k, (name, fl, fn, nl) in enumerate(self.calls):
+    def select(self, names):
+        """Keep only the named calls (for single-kernel profiling); the full
+        step still runs during warm-up so that every input is initialised."""
+        self.all_calls = self.calls
+        keep = [c for c in self.calls if c[0] in names]
+        if not keep:
+            raise SystemExit(f"--only matched nothing; names: {[c[0] for c in self.calls]}")
+        self.calls = keep
+        self.launches_per_step = sum(c[3] for c in keep)
+        self.flops = sum(c[1] for c in keep)
+
+    def run(self, events=None, calls=None):
+        for k, (name, fl, fn, nl) in enumerate(calls if calls is not None else self.calls):
             if events is not None:
                 events[k][0].record()
             fn()
@@ -277,11 +288,14 @@ def run_coda(args):
     import gemm_epilogue_fusion_tcgen05_gb300 as C
 
     step = Step(dev, with_8b=not args.no_8b)
+    warm_calls = step.calls
+    if args.only:
+        step.select(set(args.only.split(",")))
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
-        step.run()
+        step.run(calls=warm_calls)
     torch.cuda.synchronize()
     st = C.get_device_error()
     if st != 0:
@@ -334,7 +348,7 @@ def run_coda(args):
     h_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in h_ins)
     d2h = sum(t.numel() * t.element_size() for t in h_outs)
-    e2e_steps = max(2, min(args.steps, 5))
+    e2e_steps = 0 if args.only else max(2, min(args.steps, 5))
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
@@ -349,8 +363,8 @@ def run_coda(args):
         e1.record(stream)
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
-    e2e_ms /= e2e_steps
-    e2e_value = step.flops * ws / (e2e_ms * 1e-3) / 1e12
+    e2e_ms /= max(e2e_steps, 1)
+    e2e_value = step.flops * ws / (e2e_ms * 1e-3) / 1e12 if e2e_ms > 0 else None
 
     peaks, src = _peaks()
     k_dom = max(range(n), key=lambda k: per_call[k])
@@ -364,8 +378,8 @@ def run_coda(args):
         ent = tj.get("kernels", {}).get(name)
         if ent and tj.get("kernel_hash") == _kernel_hash():
             traffic = ent.get("dram_bytes_per_launch")
-    lm = [k for k in range(n) if step.calls[k][0] == "lmhead_ce"][0]
-    lm_tok_s = step.s2.M / (per_call[lm] * 1e-3)
+    lm = [k for k in range(n) if step.calls[k][0] == "lmhead_ce"]
+    lm_tok_s = step.s2.M / (per_call[lm[0]] * 1e-3) if lm else None
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
@@ -380,7 +394,7 @@ def run_coda(args):
                    "l2": "flushed before each step (512 MiB write, outside the step events)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "pct_bf16_peak": round(100 * value / ws / peak, 2),
-        "lmhead_ce_tokens_per_s": round(lm_tok_s, 1),
+        "lmhead_ce_tokens_per_s": round(lm_tok_s, 1) if lm_tok_s else None,
         "gpu_launches": step.launches_per_step * args.steps,
         "wall_s_timed_region": round(wall, 4),
         "roofline": {"kernel": name, "bound": "tensor", "achieved": round(achieved, 2),
@@ -388,12 +402,15 @@ def run_coda(args):
                      "peak_source": f"{src} bf16_tflops_sustained (timed inside a long step)",
                      "flops_per_launch": fl, "ms_per_launch": round(per_call[k_dom], 4),
                      "traffic": traffic},
-        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+        "e2e": {"value": round(e2e_value, 2) if e2e_value else None, "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clk,
         "parts_ms": {step.calls[k][0]: round(per_call[k], 4) for k in range(n)},
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if args.only:
+        line["config"]["only"] = args.only
+    if rank == 0 and not args.no_cpu_baseline and not args.only:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -491,6 +508,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-8b", action="store_true", help="leave the 8B-shaped block out of the step")
+    ap.add_argument("--only", default="", help="time only these calls (comma-separated names; "
+                    "profiling aid, not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("note: at least 3 warm-up steps are required; using 3", file=sys.stderr)
