@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libcoda.so")
 
 SOURCES = ["api.cu", "aux_kernels.cu", "gemm_plain.cu", "gemm_plain_t.cu", "gemm_fwd.cu",
            "gemm_bwd.cu"]
-HEADERS = ["internal.h", "core/ptx.cuh", "core/gemm.cuh", "core/epilogues.cuh", "core/launch.cuh"]
+HEADERS = ["internal.h", "core/ptx.cuh", "core/gemm.cuh", "core/gemm2.cuh", "core/epilogues.cuh", "core/launch.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,

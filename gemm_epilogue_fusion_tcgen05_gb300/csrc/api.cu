@@ -120,7 +120,7 @@ bool map_a(CUtensorMap* m, const void* A, int lda, int transA, int M, int K) {
 bool map_b(CUtensorMap* m, const void* B, int ldb, int transB, int N, int K) {
   if (!transB) return tmap2d(m, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, ldb, 64, 64,
                              CU_TENSOR_MAP_SWIZZLE_128B);
-  return tmap2d(m, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, ldb, 64, kTileN,
+  return tmap2d(m, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, ldb, 64, kTileN / 2,
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
 // Epilogue boxes of 32 rows: 32 bf16 (64 B), 16 bf16 (32 B), 64 bf16 (128 B), 32 fp32 (128 B).

@@ -1,0 +1,251 @@
+// Persistent tcgen05 GEMM on CTA pairs (cta_group::2): each cluster of two
+// CTAs on neighbouring SMs computes a 256 x BN tile with one
+// tcgen05.mma.cta_group::2 (M = 256) per K step, issued by the even CTA.
+// Each CTA stages its own 128 rows of A and half (BN/2 columns) of B, so per
+// SM the shared-memory traffic per MMA and the operand bytes fetched from L2
+// are half those of a single-CTA 128 x BN tile; TMEM of each CTA holds its
+// 128 accumulator rows. The epilogue is unchanged: every CTA's four epilogue
+// warps drain their own 128 x BN slice (same epilogue classes as the
+// single-CTA kernel).
+//
+// Synchronisation across the pair:
+//   full[s]   (even CTA)  both CTAs' TMA loads complete_tx here; the even
+//                          CTA's producer arms it with both CTAs' bytes
+//   empty[s]  (both)      MMA commit multicast to both CTAs frees stage s
+//   tfull[b]  (both)      MMA commit multicast: accumulator b is ready
+//   tempty[b] (even CTA)  8 arrivals (4 epilogue warps x 2 CTAs)
+//   drain     (both)      last MMA commit: nothing reads shared memory or
+//                          TMEM any more, so both CTAs may leave
+#pragma once
+#include "gemm.cuh"
+
+namespace coda {
+
+template <int BN_, bool A_MN_, bool B_MN_, class Epi_>
+struct Gemm2Traits {
+  static constexpr int BN = BN_;
+  static constexpr bool A_MN = A_MN_;
+  static constexpr bool B_MN = B_MN_;
+  using Epi = Epi_;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int A_BYTES = kBM * kBK * 2;          // this CTA's 128 rows
+  static constexpr int B_BYTES = (BN / 2) * kBK * 2;     // this CTA's half of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int EPI_BYTES = Epi::kSmemPerWarp * kEpiWarps;
+  static constexpr int BAR_BYTES = 1024;
+  static constexpr int kFit = (kSmemMax - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = kFit > 8 ? 8 : kFit;
+  static_assert(STAGES >= 3, "not enough shared memory for three pipeline stages");
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static_assert(SMEM_BYTES <= kSmemMax, "shared memory budget");
+  static constexpr int TMEM_COLS = 2 * BN;
+  static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns must be a power of two");
+  static_assert(BN % 128 == 0 && BN <= 256, "BN");
+  static constexpr uint32_t IDESC = idesc_bf16_f32(2 * kBM, BN, A_MN, B_MN);
+};
+
+template <class T>
+__global__ void __launch_bounds__(T::kThreads, 1)
+    gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ typename T::Epi::Params ep, const GemmArgs g) {
+  constexpr int S = T::STAGES;
+  constexpr int BN = T::BN;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const uint32_t sA = sbase;
+  const uint32_t sB = sbase + S * T::A_BYTES;
+  const uint32_t sEpi = sbase + S * T::STAGE_BYTES;
+  uint8_t* barp = smem + S * T::STAGE_BYTES + T::EPI_BYTES;
+  const uint32_t bars = smem_u32(barp);
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (S + s); };
+  auto tfull = [&](int i) { return bars + 8u * (2 * S + i); };
+  auto tempty = [&](int i) { return bars + 8u * (2 * S + 2 + i); };
+  const uint32_t epibar = bars + 8u * (2 * S + 4);
+  const uint32_t drainbar = bars + 8u * (2 * S + 20);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(barp + 8 * (2 * S + 21));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0 = issues the MMA, 1 = peer
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull(i), 1);
+      mbar_init(tempty(i), 2 * kEpiWarps);
+    }
+    for (int j = 0; j < 4 * kEpiWarps; ++j) mbar_init(epibar + 8u * j, 1);
+    mbar_init(drainbar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), T::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before anyone signals them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const DevError e{g.err, abort_flag, g.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int t = pair; t < g.num_tiles && ok; t += npairs) {
+        int mb, nb;
+        tile_coords(g, t, mb, nb);
+        const int m0 = mb * 2 * kBM + (int)rank * kBM;
+        const int n0 = nb * BN + (int)rank * (BN / 2);
+        for (int kb = 0; kb < g.num_kb; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, e, 21)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(full(stage), 2 * T::STAGE_BYTES);
+          const uint32_t fb = mapa_shared(full(stage), 0);
+          const uint32_t a_dst = sA + stage * T::A_BYTES;
+          const uint32_t b_dst = sB + stage * T::B_BYTES;
+          const int k0 = kb * kBK;
+          if constexpr (!T::A_MN) {
+            tma_load_2d_pair(&tmA, a_dst, fb, k0, m0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kBM / 64; ++j) tma_load_2d_pair(&tmA, a_dst + j * 8192, fb, m0 + j * 64, k0);
+          }
+          if constexpr (!T::B_MN) {
+            tma_load_2d_pair(&tmB, b_dst, fb, k0, n0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j) tma_load_2d_pair(&tmB, b_dst + j * 8192, fb, n0 + j * 64, k0);
+          }
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        for (int s = 0; s < S; ++s)
+          if (issued & (1u << s)) mbar_drain(full(s), (issued_par >> s) & 1u, 50000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0) {
+      if (leader) {
+        int stage = 0, li = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = pair; t < g.num_tiles && ok; t += npairs, ++li) {
+          const int acc = li & 1;
+          if (!mbar_wait_cluster(tempty(acc), ((li >> 1) & 1) ^ 1u, e, 22)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          for (int kb = 0; kb < g.num_kb; ++kb) {
+            if (!mbar_wait_cluster(full(stage), phase, e, 23)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_s = sA + stage * T::A_BYTES;
+            const uint32_t b_s = sB + stage * T::B_BYTES;
+#pragma unroll
+            for (int k = 0; k < kBK / kUK; ++k) {
+              const uint64_t ad = T::A_MN ? smem_desc_sw128(a_s + k * 2048, 8192, 1024)
+                                          : smem_desc_sw128(a_s + k * 32, 16, 1024);
+              const uint64_t bd = T::B_MN ? smem_desc_sw128(b_s + k * 2048, 8192, 1024)
+                                          : smem_desc_sw128(b_s + k * 32, 16, 1024);
+              mma_bf16_pair(d_tmem, ad, bd, T::IDESC, (kb | k) != 0 ? 1u : 0u);
+            }
+            mma_commit_pair(empty(stage), 0x3);
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit_pair(tfull(acc), 0x3);
+        }
+        // both CTAs learn when every MMA (which reads both CTAs' smem and
+        // writes both CTAs' TMEM) has finished
+        mma_commit_pair(drainbar, 0x3);
+        mbar_drain(drainbar, 0, 200000000ull);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 2;
+    EpiCtx ctx;
+    ctx.buf = sEpi + ew * T::Epi::kSmemPerWarp;
+    ctx.bar0 = epibar + 8u * 4 * ew;
+    ctx.phase = 0;
+    ctx.pending = 0;
+    ctx.cnt = 0;
+    ctx.lane = lane;
+    ctx.q = warp & 3;
+    ctx.e = e;
+    int li = 0;
+    for (int t = pair; t < g.num_tiles; t += npairs, ++li) {
+      int mb, nb;
+      tile_coords(g, t, mb, nb);
+      const int m0 = mb * 2 * kBM + (int)rank * kBM, n0 = nb * BN;
+      const int acc = li & 1;
+      T::Epi::template prefetch<BN>(ep, ctx, g, m0, n0);
+      bool ok = mbar_wait_cluster(tfull(acc), (li >> 1) & 1, e, 24);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * ctx.q) << 16) + acc * BN;
+      ok = T::Epi::template tile<BN>(ep, ctx, g, m0, n0, nb, taddr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
+      if (!ok) break;
+    }
+    if (lane == 0) bulk_wait<0>();
+    ctx.drain();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // copies issued before giving up may still be landing: let them finish
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 2000000ull) {
+    }
+  }
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, T::TMEM_COLS);
+  }
+}
+
+}  // namespace coda

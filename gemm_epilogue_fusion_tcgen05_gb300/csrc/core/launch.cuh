@@ -5,6 +5,7 @@
 #include <atomic>
 #include "../internal.h"
 #include "epilogues.cuh"
+#include "gemm2.cuh"
 
 namespace coda {
 
@@ -37,6 +38,57 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB,
   g.timeout_ns = lc.timeout_ns;
   const int grid = g.num_tiles < lc.num_sms ? g.num_tiles : lc.num_sms;
   gemm_kernel<T><<<grid, T::kThreads, T::SMEM_BYTES, lc.stream>>>(tmA, tmB, ep, g);
+  return cudaGetLastError();
+}
+
+// CTA-pair variant: clusters of 2, grid = 2 x min(tiles, co-resident pairs).
+template <class T>
+cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                         const typename T::Epi::Params& ep, int M, int N, int K, const LaunchCtx& lc) {
+  static std::atomic<int> max_pairs[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  dev &= 63;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(T::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = T::SMEM_BYTES;
+  cfg.stream = lc.stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int pairs_max = max_pairs[dev].load(std::memory_order_acquire);
+  if (pairs_max <= 0) {
+    e = cudaFuncSetAttribute(gemm2_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             T::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2, 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm2_kernel<T>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    pairs_max = n;
+    max_pairs[dev].store(n, std::memory_order_release);
+  }
+  GemmArgs g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
+  g.tiles_n = (N + T::BN - 1) / T::BN;
+  g.num_tiles = g.tiles_m * g.tiles_n;
+  g.num_kb = (K + kBK - 1) / kBK;
+  g.n_fast = M > N ? 1 : 0;
+  g.err = lc.err;
+  g.timeout_ns = lc.timeout_ns;
+  const int pairs = g.num_tiles < pairs_max ? g.num_tiles : pairs_max;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, gemm2_kernel<T>, tmA, tmB, ep, g);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -7,18 +7,18 @@ namespace coda {
 
 cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
   using E = EpiSwiGLUBwd;
-  using T = GemmTraits<kTileN, false, false, E>;
+  using T = Gemm2Traits<kTileN, false, false, E>;
   E::Params p;
   p.tm_y = a.tm_y;
   p.tm_dy = a.tm_dy;
   p.r = a.r;
   p.spart = a.spart;
-  return launch_gemm<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+  return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
 cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc) {
   using E = EpiNormBwd;
-  using T = GemmTraits<kTileN, false, false, E>;
+  using T = Gemm2Traits<kTileN, false, false, E>;
   E::Params p;
   p.tm_h = a.tm_h;
   p.tm_dres = a.tm_dres;
@@ -28,7 +28,7 @@ cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc) {
   p.s = a.s;
   p.dgpart = a.dgpart;
   p.has_dres = a.has_dres;
-  return launch_gemm<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+  return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
 }  // namespace coda

@@ -7,30 +7,30 @@ namespace coda {
 
 cudaError_t launch_resid_norm_stats(const ResidNormStatsArgs& a, const LaunchCtx& lc) {
   using E = EpiResidNormStats;
-  using T = GemmTraits<kTileN, false, true, E>;
+  using T = Gemm2Traits<kTileN, false, true, E>;
   E::Params p;
   p.tm_z = a.tm_z;
   p.tm_h = a.tm_h;
   p.tm_hg = a.tm_hg;
   p.gamma = a.gamma;
   p.part = a.part;
-  return launch_gemm<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+  return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
 cudaError_t launch_rowscale_swiglu(const RowScaleSwiGLUArgs& a, const LaunchCtx& lc) {
   using E = EpiRowScaleSwiGLU;
-  using T = GemmTraits<kTileN, false, true, E>;
+  using T = Gemm2Traits<kTileN, false, true, E>;
   E::Params p;
   p.tm_a = a.tm_a;
   p.tm_y = a.tm_y;
   p.r = a.r;
   p.save_y = a.save_y;
-  return launch_gemm<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+  return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
 cudaError_t launch_rope(const RopeArgs& a, const LaunchCtx& lc) {
   using E = EpiRope;
-  using T = GemmTraits<kTileN, false, true, E>;
+  using T = Gemm2Traits<kTileN, false, true, E>;
   E::Params p;
   p.tm_out = a.tm_out;
   p.r = a.r;
@@ -38,17 +38,17 @@ cudaError_t launch_rope(const RopeArgs& a, const LaunchCtx& lc) {
   p.seq_len = a.seq_len;
   p.head_dim = a.head_dim;
   p.n_rope = a.n_rope;
-  return launch_gemm<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+  return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
 cudaError_t launch_ce(const CEArgs& a, const LaunchCtx& lc) {
   using E = EpiCE;
-  using T = GemmTraits<kTileN, false, true, E>;
+  using T = Gemm2Traits<kTileN, false, true, E>;
   E::Params p;
   p.targets = a.targets;
   p.part = a.part;
   p.tlogit = a.tlogit;
-  return launch_gemm<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+  return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
 }  // namespace coda

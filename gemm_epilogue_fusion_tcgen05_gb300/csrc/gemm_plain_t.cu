@@ -7,12 +7,12 @@ namespace coda {
 template <bool AMN, bool BMN, bool F32>
 static cudaError_t plain_t_impl(const PlainArgs& a, const LaunchCtx& lc) {
   using E = EpiPlain<F32, false, false>;
-  using T = GemmTraits<kTileN, AMN, BMN, E>;
+  using T = Gemm2Traits<kTileN, AMN, BMN, E>;
   typename E::Params p;
   p.tm_c = a.tmC;
   p.tm_r = a.tmR;
   p.rowsq = nullptr;
-  return launch_gemm<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+  return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
 cudaError_t launch_plain_other(const PlainArgs& a, const LaunchCtx& lc) {
