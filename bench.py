@@ -139,7 +139,7 @@ class Step:
         M, d, f = s1.M, s1.d, s1.f
         self.i1 = mlp_block_inputs(s1, device=dev)
         self.b1 = {"h": e((M, d), bf), "hg": e((M, d), bf), "part": e((C.col_tiles(d), M), f32),
-                   "r": e((M,), f32), "a": e((M, f), bf), "y": e((M, 2 * f), bf),
+                   "r": e((M,), f32), "a": e((M, f), bf), "y": e((M, 2 * f), f32),
                    "out": e((M, d), bf), "dyhat": e((M, 2 * f), bf),
                    "spart": e((C.col_tiles(f), M), f32), "s": e((M,), f32), "dh": e((M, d), bf),
                    "dgpart": e((C.row_tiles32(M), d), f32), "dgamma": e((d,), f32),
@@ -162,9 +162,10 @@ class Step:
             M4, d4, f4, n4 = s4.M, s4.d, s4.f, s4.n_qkv
             self.b4 = {"h": e((M4, d4), bf), "hg": e((M4, d4), bf),
                        "part": e((C.col_tiles(d4), M4), f32), "r": e((M4,), f32),
-                       "a": e((M4, f4), bf), "y": e((M4, 2 * f4), bf), "out": e((M4, d4), bf),
+                       "a": e((M4, f4), bf), "y": e((M4, 2 * f4), f32), "out": e((M4, d4), bf),
                        "outg": e((M4, d4), bf), "part1": e((C.col_tiles(d4), M4), f32),
-                       "r1": e((M4,), f32), "qkv": e((M4, n4), bf), "dqh": e((M4, n4), bf),
+                       "r1": e((M4,), f32), "qkv": e((M4, n4), bf), "qkv32": e((M4, n4), f32),
+                       "dqh": e((M4, n4), bf),
                        "s1": e((M4,), f32), "dout": e((M4, d4), bf),
                        "dgp1": e((C.row_tiles32(M4), d4), f32), "dgamma1": e((d4,), f32),
                        "dWqkv": e((d4, n4), f32), "dyhat": e((M4, 2 * f4), bf),
@@ -220,9 +221,10 @@ class Step:
                                                      b4["out"], b4["outg"], b4["part1"]))
             add("8b.row_rms1", 0, lambda: C.coda_row_rms(b4["part1"], b4["r1"], d4, 1e-6))
             add("8b.gemm_rope", 2 * M4 * d4 * n4,
-                lambda: C.coda_gemm_rope(b4["outg"], i4["Wqkv"], b4["r1"], cs, sl, hd, nr, b4["qkv"]))
+                lambda: C.coda_gemm_rope(b4["outg"], i4["Wqkv"], b4["r1"], cs, sl, hd, nr, b4["qkv"],
+                                         b4["qkv32"]))
             add("8b.rope_bwd", 0,
-                lambda: C.coda_gemm_rope_bwd(i4["dqkv"], b4["qkv"], b4["r1"], cs, sl, hd, nr,
+                lambda: C.coda_gemm_rope_bwd(i4["dqkv"], b4["qkv32"], b4["r1"], cs, sl, hd, nr,
                                              b4["dqh"], b4["s1"], d4))
             add("8b.gemm_resid_norm_stats_bwd(Wqkv)", 2 * M4 * n4 * d4,
                 lambda: C.coda_gemm_resid_norm_stats_bwd(b4["dqh"], i4["Wqkv"], b4["out"],

@@ -40,7 +40,7 @@ EXPORTS = {
     "coda_gemm_resid_norm_stats": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "coda_row_rms": (_I, [_P, _I, _I, _I, _F, _P, _P]),
     "coda_gemm_rowscale_swiglu": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
-    "coda_gemm_rope": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P]),
+    "coda_gemm_rope": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _P]),
     "coda_rope_table": (_I, [_P, _I, _I, _D, _P]),
     "coda_lmhead_ce_workspace_size": (_Z, [_I, _I]),
     "coda_lmhead_ce": (_I, [_P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _P]),
@@ -179,7 +179,7 @@ def coda_gemm_rowscale_swiglu(hg, W1, r, a, y_save=None, stream=None):
     _req(a, bf16, "a")
     _req(r, f32, "r", 1)
     if y_save is not None:
-        _req(y_save, bf16, "y_save")
+        _req(y_save, f32, "y_save")
     _check(lib().coda_gemm_rowscale_swiglu(_ptr(hg), _ptr(W1), _ptr(r), _ptr(a), _ptr(y_save),
                                            M, two_f, K, _stream(stream)))
 
@@ -190,14 +190,16 @@ def coda_rope_table(cos_sin, seq_len: int, head_dim: int, theta: float, stream=N
 
 
 def coda_gemm_rope(A, W, r, cos_sin, seq_len: int, head_dim: int, n_rope_cols: int, out,
-                   stream=None):
+                   out_f32=None, stream=None):
     M, K = A.shape
     N = W.shape[1]
     _req(A, bf16, "A")
     _req(W, bf16, "W")
     _req(out, bf16, "out")
+    if out_f32 is not None:
+        _req(out_f32, f32, "out_f32")
     _check(lib().coda_gemm_rope(_ptr(A), _ptr(W), _ptr(r), _ptr(cos_sin), seq_len, head_dim,
-                                n_rope_cols, _ptr(out), M, N, K, _stream(stream)))
+                                n_rope_cols, _ptr(out), _ptr(out_f32), M, N, K, _stream(stream)))
 
 
 def coda_lmhead_ce_workspace_size(M: int, V: int) -> int:
@@ -222,8 +224,9 @@ def coda_lmhead_ce(hidden, W, targets, lse, loss, ws, stream=None):
 def coda_gemm_rowscale_swiglu_bwd(dout, W2, y, r, dyhat, spart, stream=None):
     M, d = dout.shape
     f = W2.shape[0]
-    for t, n in ((dout, "dout"), (W2, "W2"), (y, "y"), (dyhat, "dyhat")):
+    for t, n in ((dout, "dout"), (W2, "W2"), (dyhat, "dyhat")):
         _req(t, bf16, n)
+    _req(y, f32, "y")
     _req(spart, f32, "spart")
     _check(lib().coda_gemm_rowscale_swiglu_bwd(_ptr(dout), _ptr(W2), _ptr(y), _ptr(r), _ptr(dyhat),
                                                _ptr(spart), M, f, d, _stream(stream)))
@@ -253,6 +256,8 @@ def coda_col_reduce(part, out, stream=None):
 def coda_gemm_rope_bwd(dqkv_rot, qkv_rot, r, cos_sin, seq_len: int, head_dim: int,
                        n_rope_cols: int, dqkv_hat, s, d: int, stream=None):
     M, N = dqkv_rot.shape
+    _req(dqkv_rot, bf16, "dqkv_rot")
+    _req(qkv_rot, f32, "qkv_rot")
     _check(lib().coda_gemm_rope_bwd(_ptr(dqkv_rot), _ptr(qkv_rot), _ptr(r), _ptr(cos_sin), seq_len,
                                     head_dim, n_rope_cols, _ptr(dqkv_hat), _ptr(s), M, N, d,
                                     _stream(stream)))

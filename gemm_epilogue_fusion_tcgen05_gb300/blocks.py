@@ -42,7 +42,7 @@ def mlp_block_fwd(x, z, W0, W1, W2, gamma, eps: float = 1e-6, save_y: bool = Tru
     part = b.get("part") if "part" in b else _e((col_tiles(d), M), f32, dev)
     r = b.get("r") if "r" in b else _e((M,), f32, dev)
     a = b.get("a") if "a" in b else _e((M, two_f // 2), bf16, dev)
-    y = (b.get("y") if "y" in b else _e((M, two_f), bf16, dev)) if save_y else None
+    y = (b.get("y") if "y" in b else _e((M, two_f), f32, dev)) if save_y else None
     out = b.get("out") if "out" in b else _e((M, d), bf16, dev)
     coda_gemm_resid_norm_stats(x, W0, z, gamma, h, hg, part)
     coda_row_rms(part, r, d, eps)
@@ -118,19 +118,20 @@ def block8b_fwd(inp: Dict[str, torch.Tensor], seq_len: int, head_dim: int, n_rop
     part = _e((col_tiles(d), M), f32, dev)
     r = _e((M,), f32, dev)
     a = _e((M, two_f // 2), bf16, dev)
-    y = _e((M, two_f), bf16, dev)
+    y = _e((M, two_f), f32, dev)
     out, outg = _e((M, d), bf16, dev), _e((M, d), bf16, dev)
     part1 = _e((col_tiles(d), M), f32, dev)
     r1 = _e((M,), f32, dev)
     qkv = _e((M, nq), bf16, dev)
+    qkv32 = _e((M, nq), f32, dev)
     coda_gemm_resid_norm_stats(o, inp["Wo"], z, inp["gamma2"], h, hg, part)
     coda_row_rms(part, r, d, eps)
     coda_gemm_rowscale_swiglu(hg, inp["W1"], r, a, y)
     coda_gemm_resid_norm_stats(a, inp["W2"], h, inp["gamma1"], out, outg, part1)
     coda_row_rms(part1, r1, d, eps)
-    coda_gemm_rope(outg, inp["Wqkv"], r1, cos_sin, seq_len, head_dim, n_rope_cols, qkv)
+    coda_gemm_rope(outg, inp["Wqkv"], r1, cos_sin, seq_len, head_dim, n_rope_cols, qkv, qkv32)
     return {"h": h, "hg": hg, "r": r, "a": a, "y": y, "out": out, "outg": outg, "r1": r1,
-            "qkv": qkv}
+            "qkv": qkv, "qkv32": qkv32}
 
 
 def block8b_bwd(fwd: Dict[str, torch.Tensor], inp: Dict[str, torch.Tensor], seq_len: int,
@@ -145,7 +146,7 @@ def block8b_bwd(fwd: Dict[str, torch.Tensor], inp: Dict[str, torch.Tensor], seq_
     dev = o.device
     dqh = _e((M, nq), bf16, dev)
     s1 = _e((M,), f32, dev)
-    coda_gemm_rope_bwd(inp["dqkv"], fwd["qkv"], fwd["r1"], cos_sin, seq_len, head_dim,
+    coda_gemm_rope_bwd(inp["dqkv"], fwd["qkv32"], fwd["r1"], cos_sin, seq_len, head_dim,
                        n_rope_cols, dqh, s1, d)
     dout = _e((M, d), bf16, dev)
     dgp1 = _e((row_tiles32(M), d), f32, dev)
@@ -174,6 +175,7 @@ def block8b_bwd(fwd: Dict[str, torch.Tensor], inp: Dict[str, torch.Tensor], seq_
     coda_gemm(o, dh, dWo, transA=True)
     do = _e((M, d), bf16, dev)
     coda_gemm(dh, inp["Wo"], do, transB=True)
-    return {"dqkv_hat": dqh, "s1": s1, "dout": dout, "dgamma1": dgamma1, "dWqkv": dWqkv,
+    return {"dqkv_hat": dqh, "s1": s1, "dout": dout, "dgamma1": dgamma1, "dgpart1": dgp1,
+            "dgpart2": dgp2, "dWqkv": dWqkv,
             "dyhat": dyhat, "s": s, "dW2": dW2, "dh": dh, "dz": dh, "dgamma2": dgamma2,
             "dW1": dW1, "dWo": dWo, "do": do}

@@ -214,10 +214,12 @@ struct EpiResidNormStats {
 // GEMM 2 with the delayed row scale and the pairwise SwiGLU map ("Reading
 // notes on CODA", s2: y[i,j] = r[i] h3[i,j]; pairwise activations on
 // adjacent accumulator values; pith Fig. 7 caption):
-//   y = r[m] * acc ; a_k = silu(y_2k) * y_2k+1 (stored) ; y optionally stored
+//   y = r[m] * acc ; a_k = silu(y_2k) * y_2k+1 (bf16) ; y optionally saved in
+//   fp32 for the backward (its relocated RMSNorm statistic sums 2f products
+//   with heavy cancellation, which bf16 storage of y would dominate)
 struct EpiRowScaleSwiGLU {
   static constexpr int kABufB = 1024;  // 32 rows x 16 bf16 (32-byte rows)
-  static constexpr int kYBufB = 2048;  // 32 rows x 32 bf16
+  static constexpr int kYBufB = 4096;  // 32 rows x 32 fp32 (128-byte rows)
   static constexpr int kSmemPerWarp = 2 * kABufB + 2 * kYBufB;
   struct Params {
     CUtensorMap tm_a, tm_y;
@@ -251,7 +253,13 @@ struct EpiRowScaleSwiGLU {
       }
       st_shared_v4(abuf + swz<32>(c.lane, 0), ap[0], ap[1], ap[2], ap[3]);
       st_shared_v4(abuf + swz<32>(c.lane, 1), ap[4], ap[5], ap[6], ap[7]);
-      if (p.save_y) stage_bf16x32(ybuf, c.lane, v);
+      if (p.save_y) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(ybuf + swz<128>(c.lane, k), __float_as_uint(v[4 * k]),
+                       __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
+                       __float_as_uint(v[4 * k + 3]));
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
@@ -271,14 +279,17 @@ struct EpiRowScaleSwiGLU {
 //   v = r[m] * acc ; for columns < n_rope, inside each head_dim-wide head,
 //   (v_2i, v_2i+1) -> (v_2i c - v_2i+1 s, v_2i s + v_2i+1 c),
 //   (c, s) = cos_sin[pos(m), i], pos(m) = m mod seq_len
+// Output bf16; optionally also an fp32 copy kept for the backward's
+// relocated RMSNorm statistic.
 struct EpiRope {
-  static constexpr int kBufB = 2048;
-  static constexpr int kSmemPerWarp = 2 * kBufB;
+  static constexpr int kBufB = 2048;   // 32 rows x 32 bf16
+  static constexpr int kSBufB = 4096;  // 32 rows x 32 fp32
+  static constexpr int kSmemPerWarp = 2 * kBufB + 2 * kSBufB;
   struct Params {
-    CUtensorMap tm_out;
+    CUtensorMap tm_out, tm_save;
     const float* r;        // nullable: no row scale
     const float2* cs;      // [seq_len, head_dim/2] (cos, sin)
-    int seq_len, head_dim, n_rope;
+    int seq_len, head_dim, n_rope, save;
   };
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params&, EpiCtx&, const GemmArgs&, int, int) {}
@@ -293,6 +304,7 @@ struct EpiRope {
     for (int ch = 0; ch < NCH; ++ch) {
       const int b = c.cnt & 1;
       const uint32_t buf = c.buf + b * kBufB;
+      const uint32_t sbuf = c.buf + 2 * kBufB + b * kSBufB;
       c.stores_read_done();
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
@@ -312,10 +324,18 @@ struct EpiRope {
         }
       }
       stage_bf16x32(buf, c.lane, v);
+      if (p.save) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(sbuf + swz<128>(c.lane, k), __float_as_uint(v[4 * k]),
+                       __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
+                       __float_as_uint(v[4 * k + 3]));
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
         tma_store_2d(&p.tm_out, buf, col0, m0 + 32 * c.q);
+        if (p.save) tma_store_2d(&p.tm_save, sbuf, col0, m0 + 32 * c.q);
         bulk_commit();
       }
       ++c.cnt;
@@ -386,22 +406,35 @@ struct EpiCE {
 // pith Fig. 7: the SwiGLU backward maps one incoming gradient to both paired
 // inputs; "Eliminating the RMSNorm backward kernel": the row statistic is
 // accumulated here):
-//   da = acc ; (g, u) = saved y pair ; dg = da u sig(g) (1 + g (1 - sig(g)))
-//   du = da silu(g) ; spart[nb, m] = sum (dg g + du u) ; dyhat = r (dg, du)
+//   da = acc ; (g, u) = saved y pair (fp32) ; sg = sigmoid(g)
+//   dg = da u sg (1 + g (1 - sg)) ; du = da g sg
+//   spart[nb, m] = sum (dg g + du u) ; dyhat = r (dg, du) (bf16)
+// Per 32-column chunk of da: two fp32 boxes of y (64 columns) in, one bf16
+// box of dyhat (64 columns) out.
 struct EpiSwiGLUBwd {
-  static constexpr int kBufB = 4096;  // 32 rows x 64 bf16 (y in, dyhat out)
-  static constexpr int kSmemPerWarp = 2 * kBufB;
+  static constexpr int kYBufB = 8192;   // 2 boxes of 32 rows x 32 fp32
+  static constexpr int kOBufB = 4096;   // 32 rows x 64 bf16
+  static constexpr int kSetB = kYBufB + kOBufB;
+  static constexpr int kSmemPerWarp = 2 * kSetB;
   struct Params {
     CUtensorMap tm_y, tm_dy;
     const float* r;
     float* spart;  // [tiles_n, M]
   };
+  static __device__ __forceinline__ void load_y(const Params& p, EpiCtx& c, int b, int col0, int m0) {
+    const uint32_t ybuf = c.buf + b * kSetB;
+    if (c.lane == 0) {
+      mbar_arrive_expect_tx(c.bar(b), kYBufB);
+      tma_load_2d(&p.tm_y, ybuf, c.bar(b), col0, m0 + 32 * c.q);
+      tma_load_2d(&p.tm_y, ybuf + 4096, c.bar(b), col0 + 32, m0 + 32 * c.q);
+    }
+    c.pending |= 1u << b;
+  }
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
                                                   int m0, int n0) {
     c.stores_read_done();
-    const int b = c.cnt & 1;
-    c.load(&p.tm_y, b, c.buf + b * kBufB, 2 * n0, m0 + 32 * c.q, kBufB);
+    load_y(p, c, c.cnt & 1, 2 * n0, m0);
   }
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
@@ -412,22 +445,26 @@ struct EpiSwiGLUBwd {
     float ss = 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
       const int b = c.cnt & 1;
-      const uint32_t buf = c.buf + b * kBufB;
+      const uint32_t ybuf = c.buf + b * kSetB;
+      const uint32_t obuf = ybuf + kYBufB;
       c.stores_read_done();
-      if (ch + 1 < NCH)
-        c.load(&p.tm_y, b ^ 1, c.buf + (b ^ 1) * kBufB, 2 * (n0 + (ch + 1) * 32), m0 + 32 * c.q, kBufB);
+      if (ch + 1 < NCH) load_y(p, c, b ^ 1, 2 * (n0 + (ch + 1) * 32), m0);
       float da[32];
       tmem_ld32(taddr + ch * 32, da);
       if (!c.wait(b, 12)) return false;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {  // 16-byte chunk k = pairs 4k .. 4k+3
-        const uint32_t addr = buf + swz<128>(c.lane, k);
-        const uint4 u = ld_shared_v4(addr);
-        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+      for (int k = 0; k < 8; ++k) {  // output chunk k = pairs 4k .. 4k+3
+        const uint32_t yb = ybuf + (k >> 2) * 4096;
+        const uint4 y0 = ld_shared_v4(yb + swz<128>(c.lane, 2 * (k & 3)));
+        const uint4 y1 = ld_shared_v4(yb + swz<128>(c.lane, 2 * (k & 3) + 1));
+        const float gy[4] = {__uint_as_float(y0.x), __uint_as_float(y0.z), __uint_as_float(y1.x),
+                             __uint_as_float(y1.z)};
+        const float uy[4] = {__uint_as_float(y0.y), __uint_as_float(y0.w), __uint_as_float(y1.y),
+                             __uint_as_float(y1.w)};
         uint32_t outw[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const float gg = bf16_lo(in[t]), uu = bf16_hi(in[t]);
+          const float gg = gy[t], uu = uy[t];
           const float sg = sigmoidf_fast(gg);
           const float d = da[4 * k + t];
           const float dg = d * uu * sg * (1.0f + gg * (1.0f - sg));
@@ -435,12 +472,12 @@ struct EpiSwiGLUBwd {
           ss = fmaf(dg, gg, fmaf(du, uu, ss));
           outw[t] = pack_bf16(rr * dg, rr * du);
         }
-        st_shared_v4(addr, outw[0], outw[1], outw[2], outw[3]);
+        st_shared_v4(obuf + swz<128>(c.lane, k), outw[0], outw[1], outw[2], outw[3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
-        tma_store_2d(&p.tm_dy, buf, 2 * (n0 + ch * 32), m0 + 32 * c.q);
+        tma_store_2d(&p.tm_dy, obuf, 2 * (n0 + ch * 32), m0 + 32 * c.q);
         bulk_commit();
       }
       ++c.cnt;

@@ -33,6 +33,8 @@ cudaError_t launch_rope(const RopeArgs& a, const LaunchCtx& lc) {
   using T = Gemm2Traits<kTileN, false, true, E>;
   E::Params p;
   p.tm_out = a.tm_out;
+  p.tm_save = a.tm_save;
+  p.save = a.save;
   p.r = a.r;
   p.cs = a.cs;
   p.seq_len = a.seq_len;

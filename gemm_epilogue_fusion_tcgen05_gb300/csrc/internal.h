@@ -44,10 +44,10 @@ struct RowScaleSwiGLUArgs {
 cudaError_t launch_rowscale_swiglu(const RowScaleSwiGLUArgs& a, const LaunchCtx& lc);
 
 struct RopeArgs {
-  CUtensorMap tmA, tmB, tm_out;
+  CUtensorMap tmA, tmB, tm_out, tm_save;
   const float* r;
   const float2* cs;
-  int seq_len, head_dim, n_rope;
+  int seq_len, head_dim, n_rope, save;
   int M, N, K;
 };
 cudaError_t launch_rope(const RopeArgs& a, const LaunchCtx& lc);
@@ -93,7 +93,7 @@ cudaError_t launch_col_reduce(const float* part, int nparts, int N, float* out, 
 cudaError_t launch_ce_combine(const float2* part, int nparts, const float* tlogit, const int* targets,
                               int M, int V, float* lse, float* loss, int* err, cudaStream_t st);
 cudaError_t launch_rope_table(float2* cs, int seq_len, int head_dim, double theta, cudaStream_t st);
-cudaError_t launch_rope_bwd(const bf16* d, const bf16* q, const float* r, const float2* cs,
+cudaError_t launch_rope_bwd(const bf16* d, const float* q, const float* r, const float2* cs,
                             int seq_len, int head_dim, int n_rope, bf16* out, float* s, int M, int N,
                             float inv_d, cudaStream_t st);
 cudaError_t launch_bounded_wait_probe(int* err, unsigned long long timeout_ns, cudaStream_t st);

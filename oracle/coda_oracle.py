@@ -143,12 +143,14 @@ def mlp_fwd_reparam(x, z, W0, W1, W2, gamma, eps: float = EPS,
                          mean of squares is taken on D before the RMSNorm
                          weight multiplies it)
         auxiliary:       r = 1/sqrt(mean(h^2) + eps)
-        GEMM 2 epilogue: y = r * (hg W1)  (delayed row scale, stored),
-                         a = silu(y_gate) * y_up (stored)
+        GEMM 2 epilogue: y = r * (hg W1)  (delayed row scale, saved for the
+                         backward in fp32), a = silu(y_gate) * y_up (stored)
         GEMM 3:          out = a W2
-    With store_bf16, each stored tensor is rounded to bf16 where the rewritten
-    kernels write it; its consumers read the rounded value, the statistics are
-    taken before rounding."""
+    With store_bf16, each tensor the rewritten kernels store in bf16 (h, hg,
+    a, out) is rounded to bf16 where it is written; its consumers read the
+    rounded value, the statistics are taken before rounding. The saved y is
+    kept at full precision (its fp32 storage error is far below every
+    tolerance)."""
     st = _store(store_bf16)
     x, z, W0, W1, W2, gamma = (np.asarray(t, dtype=f64) for t in (x, z, W0, W1, W2, gamma))
     h_acc = x @ W0 + z
@@ -157,7 +159,7 @@ def mlp_fwd_reparam(x, z, W0, W1, W2, gamma, eps: float = EPS,
     hg = st(h_acc * gamma[None, :])
     y_acc = r[:, None] * (hg @ W1)
     a = st(swiglu(y_acc))
-    y = st(y_acc)
+    y = y_acc
     out = st(a @ W2)
     return {"h": h, "r": r, "hg": hg, "y": y, "a": a, "out": out}
 
@@ -376,6 +378,80 @@ def block8b_bwd(fwd, o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres, pos,
     return {"dqkv_pre": dqkv_pre, "dWqkv": dWqkv, "dgamma1": dgamma1, "s1": s1,
             "dout": dout, "da": da, "dW2": dW2, "dy": dy, "dW1": dW1, "dgamma2": dgamma2,
             "s": s, "dh": dh, "dz": dh, "do": do, "dWo": dWo}
+
+
+def block8b_fwd_reparam(o, z, Wo, W1, W2, gamma2, gamma1, Wqkv, pos, n_rope_cols: int,
+                        head_dim: int, theta: float = ROPE_THETA, eps: float = EPS,
+                        store_bf16: bool = False):
+    """The pages' rewritten form of ``block8b_fwd`` [notes s2; pith Fig. 4 and
+    Fig. 7]: each RMSNorm is split into a GEMM-epilogue statistic on the
+    unscaled residual sum and a delayed row scale in the next GEMM's epilogue:
+        h = o Wo + z ; hg = h * gamma2 ; r = rms factor of h
+        y = r (hg W1) ; a = silu(g) u
+        out = a W2 + h ; outg = out * gamma1 ; r1 = rms factor of out
+        qkv = RoPE(r1 (outg Wqkv))
+    With store_bf16, the tensors the rewritten kernels store in bf16 (h, hg,
+    a, out, outg, qkv) are rounded where they are written and read back
+    rounded; y and the copy of qkv kept for the backward's statistic
+    (``qkv_save``) stay at full precision (saved in fp32)."""
+    st = _store(store_bf16)
+    o, z, Wo, W1, W2, gamma2, gamma1, Wqkv = (np.asarray(t, dtype=f64) for t in
+                                               (o, z, Wo, W1, W2, gamma2, gamma1, Wqkv))
+    h_acc = o @ Wo + z
+    r = rms_factor(h_acc, eps)
+    h = st(h_acc)
+    hg = st(h_acc * gamma2[None, :])
+    y = r[:, None] * (hg @ W1)
+    a = st(swiglu(y))
+    out_acc = a @ W2 + h
+    r1 = rms_factor(out_acc, eps)
+    out = st(out_acc)
+    outg = st(out_acc * gamma1[None, :])
+    qkv_acc = rope_apply(r1[:, None] * (outg @ Wqkv), pos, n_rope_cols, head_dim, theta)
+    return {"h": h, "hg": hg, "r": r, "y": y, "a": a, "out": out, "outg": outg, "r1": r1,
+            "qkv": st(qkv_acc), "qkv_save": qkv_acc}
+
+
+def block8b_bwd_reparam(fwd, o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres, pos,
+                        n_rope_cols: int, head_dim: int, theta: float = ROPE_THETA,
+                        store_bf16: bool = False, stat_only: bool = False):
+    """Reverse-fused backward of ``block8b_fwd_reparam`` [notes s3]:
+        dqh = r1 R^T dqkv (stored) ; s1 = (1/d) sumcols(dqkv * qkv_save)
+        P1 = dqh Wqkv^T ; dout = gamma1 P1 - r1^2 s1 out + dres (stored)
+        dgamma1 = sum_rows P1 * out ; dWqkv = outg^T dqh
+        da = dout W2^T ; dy from the SwiGLU pair rule ; s = (1/d) sumcols(dy * y)
+        dyhat = r dy (stored) ; P = dyhat W1^T
+        dh = gamma2 P - r^2 s h + dout (stored) ; dgamma2 = sum_rows P * h
+        dW2 = a^T dout ; dW1 = hg^T dyhat ; dWo = o^T dh ; do = dh Wo^T
+    ``stat_only`` stops after s1 and s (and the tensors they need)."""
+    st = _store(store_bf16)
+    o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres = (
+        np.asarray(t, dtype=f64) for t in (o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres))
+    d = fwd["h"].shape[1]
+    r, r1 = fwd["r"], fwd["r1"]
+    dqh = st(r1[:, None] * rope_apply(dqkv, pos, n_rope_cols, head_dim, theta, inverse=True))
+    s1 = np.sum(dqkv * fwd["qkv_save"], axis=1) / d
+    P1 = dqh @ Wqkv.T
+    dout = st(gamma1[None, :] * P1 - (r1 * r1 * s1)[:, None] * fwd["out"] + dres)
+    da = dout @ W2.T
+    y = fwd["y"]
+    g = y[:, 0::2]
+    u = y[:, 1::2]
+    dy = np.empty_like(y)
+    dy[:, 0::2] = da * u * silu_grad(g)
+    dy[:, 1::2] = da * silu(g)
+    s = np.sum(dy * y, axis=1) / d
+    dyhat = st(r[:, None] * dy)
+    res = {"dqkv_hat": dqh, "s1": s1, "dout": dout, "dy": dy, "s": s, "dyhat": dyhat}
+    if stat_only:
+        return res
+    P = dyhat @ W1.T
+    dh = st(gamma2[None, :] * P - (r * r * s)[:, None] * fwd["h"] + dout)
+    res.update({"dgamma1": np.sum(P1 * fwd["out"], axis=0), "dWqkv": fwd["outg"].T @ dqh,
+                "dW2": fwd["a"].T @ dout, "dh": dh, "dz": dh,
+                "dgamma2": np.sum(P * fwd["h"], axis=0), "dW1": fwd["hg"].T @ dyhat,
+                "dWo": o.T @ dh, "do": st(dh @ Wo.T)})
+    return res
 
 
 def to64(t) -> np.ndarray:

@@ -9,6 +9,12 @@ import torch
 
 TOL_BF16 = 2e-2
 TOL_F32 = 1e-3
+# The RMSNorm-backward statistic s sums a row of products with heavy
+# cancellation; the bf16 rounding of the GEMM operand it is built from (hg,
+# dout, qkv) moves it ~1e-3 relative to the exact fp64 value. It meets 1e-3
+# against the oracle's storage-rounded form, and this bound against the exact
+# canonical form.
+TOL_S_EXACT = 5e-3
 
 
 def to64(t):

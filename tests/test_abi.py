@@ -77,7 +77,7 @@ def test_invalid_arguments_rejected_on_host(L):
     # swiglu: two_f must be a multiple of 16
     assert L.coda_gemm_rowscale_swiglu(ok, ok, ok, ok, None, 64, 24, 64, None) == 1
     # rope: n_rope not a multiple of head_dim
-    assert L.coda_gemm_rope(ok, ok, None, ok, 128, 128, 100, ok, 64, 256, 64, None) == 1
+    assert L.coda_gemm_rope(ok, ok, None, ok, 128, 128, 100, ok, None, 64, 256, 64, None) == 1
     # CE: workspace too small
     assert L.coda_lmhead_ce(ok, ok, ok, ok, ok, ok, 16, 64, 512, 64, None) == 1
     assert b"workspace" in L.coda_last_error_string()

@@ -16,7 +16,7 @@ import torch
 
 from coda_inputs import WORKLOADS, mlp_block_inputs, lmhead_inputs, block8b_inputs, positions
 from oracle import coda_oracle as O
-from tests._util import TOL_BF16, TOL_F32, assert_close, to64
+from tests._util import TOL_BF16, TOL_F32, TOL_S_EXACT, assert_close, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -85,6 +85,7 @@ def test_llama1b_backward_full_oracle(coda):
     rb = O.mlp_bwd(ref, n["x"], n["W0"], n["W1"], n["W2"], n["gamma"], n["dout"])
     for k in ("dx", "dz", "dW0", "dW1", "dW2", "dgamma"):
         assert_close(k, bw[k], rb[k], TOL_BF16)
+    assert_close("s (exact oracle)", bw["s"], rb["s"], TOL_S_EXACT)
     del ref, rb
     st = O.mlp_fwd_reparam(n["x"], n["z"], n["W0"], n["W1"], n["W2"], n["gamma"], store_bf16=True)
     sb = O.mlp_bwd_reparam(st, n["x"], n["W0"], n["W1"], n["W2"], n["gamma"], n["dout"],
@@ -134,8 +135,31 @@ def test_llama8b_block_full_size(coda):
         assert_close(k, fw[k][ri], want, tol)
     for k in ("dout", "dz", "do"):
         assert_close(k, bw[k][ri], rb[k], TOL_BF16)
-    assert_close("s1", bw["s1"][ri], rb["s1"], 1e-2)
-    assert_close("s", bw["s"][ri], rb["s"], 1e-2)
+    assert_close("s1 (exact oracle)", bw["s1"][ri], rb["s1"], TOL_S_EXACT)
+    assert_close("s (exact oracle)", bw["s"][ri], rb["s"], TOL_S_EXACT)
+    fr = O.block8b_fwd_reparam(n["o"], n["z"], n["Wo"], n["W1"], n["W2"], n["gamma2"], n["gamma1"],
+                               n["Wqkv"], pos, sh.n_rope_cols, sh.head_dim, sh.theta, store_bf16=True)
+    br = O.block8b_bwd_reparam(fr, n["o"], n["Wo"], n["W1"], n["W2"], n["gamma2"], n["gamma1"],
+                               n["Wqkv"], n["dqkv"], n["dres"], pos, sh.n_rope_cols, sh.head_dim,
+                               sh.theta, store_bf16=True, stat_only=True)
+    assert_close("s1 (storage-rounded oracle)", bw["s1"][ri], br["s1"], TOL_F32)
+    assert_close("s (storage-rounded oracle)", bw["s"][ri], br["s"], TOL_F32)
+    # dgamma: the column reduction of its per-32-row partials, and the
+    # partials of the two sampled 32-row blocks against the oracle
+    for k in ("1", "2"):
+        gp = to64(bw["dgpart" + k])
+        assert_close(f"dgamma{k} = sum of partials", bw["dgamma" + k], gp.sum(0), 1e-5)
+    for blk_rows, j in ((np.arange(0, 32), 0), (np.arange(sh.M - 32, sh.M), sh.M // 32 - 1)):
+        nb = {k: O.to64(v[blk_rows]) if v.dim() == 2 and v.shape[0] == sh.M else O.to64(v)
+              for k, v in inp.items()}
+        pb = positions(sh.M, sh.seq_len).numpy()[blk_rows]
+        fb = O.block8b_fwd(nb["o"], nb["z"], nb["Wo"], nb["W1"], nb["W2"], nb["gamma2"],
+                           nb["gamma1"], nb["Wqkv"], pb, sh.n_rope_cols, sh.head_dim, sh.theta)
+        bb = O.block8b_bwd(fb, nb["o"], nb["Wo"], nb["W1"], nb["W2"], nb["gamma2"], nb["gamma1"],
+                           nb["Wqkv"], nb["dqkv"], nb["dres"], pb, sh.n_rope_cols, sh.head_dim,
+                           sh.theta)
+        assert_close(f"dgamma1 partial of rows {blk_rows[0]}..", bw["dgpart1"][j], bb["dgamma1"], TOL_BF16)
+        assert_close(f"dgamma2 partial of rows {blk_rows[0]}..", bw["dgpart2"][j], bb["dgamma2"], TOL_BF16)
     # weight gradients at full size through dW v = A^T (G v)
     _proj_check("dWqkv", bw["dWqkv"], fw["outg"], bw["dqkv_hat"], 1)
     _proj_check("dW2", bw["dW2"], fw["a"], bw["dout"], 2)

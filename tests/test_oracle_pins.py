@@ -217,7 +217,7 @@ def test_storage_rounded_mode_rounds_stored_tensors_only():
     inp = rand_block(M=4, d=16, f=8, seed=8)
     fr = O.mlp_fwd_reparam(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"],
                            store_bf16=True)
-    for k in ("h", "hg", "y", "a", "out"):
+    for k in ("h", "hg", "a", "out"):
         assert np.array_equal(fr[k], O.bf16_round(fr[k])), k
     fe = O.mlp_fwd_reparam(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"])
     assert rel(fr["r"], fe["r"]) < 1e-15          # statistics come from the unrounded h
@@ -413,6 +413,31 @@ def test_block8b_qkv_statistic_through_rotation():
     b = np.sum(inp["dqkv"] * fw["qkv"], axis=1)
     assert rel(a, b) < 1e-13
     assert rel(bw["s1"], b / 8) < 1e-12
+
+
+def test_block8b_reparam_equals_canonical():
+    # delayed row scales through both RMSNorms, s and s1 from the relocated form
+    inp, nrope, hd = rand_8b(M=5, d=16, f=12, hd=8, nq=2, nkv=1, seed=18)
+    pos = np.array([0, 1, 5, 100, 4095])
+    args = (inp["o"], inp["z"], inp["Wo"], inp["W1"], inp["W2"], inp["gamma2"], inp["gamma1"],
+            inp["Wqkv"], pos, nrope, hd)
+    fc = O.block8b_fwd(*args)
+    fr = O.block8b_fwd_reparam(*args)
+    for k in ("h", "r", "y", "a", "out", "r1", "qkv"):
+        assert rel(fr[k], fc[k]) < 1e-12, k
+    bargs = (inp["o"], inp["Wo"], inp["W1"], inp["W2"], inp["gamma2"], inp["gamma1"], inp["Wqkv"],
+             inp["dqkv"], inp["dres"], pos, nrope, hd)
+    bc = O.block8b_bwd(fc, *bargs)
+    br = O.block8b_bwd_reparam(fr, *bargs)
+    for k in ("s1", "s", "dout", "dz", "do", "dWo", "dW1", "dW2", "dWqkv", "dgamma1", "dgamma2"):
+        assert rel(br[k], bc[k]) < 1e-11, k
+    so = O.block8b_bwd_reparam(fr, *bargs, stat_only=True)
+    assert rel(so["s"], bc["s"]) < 1e-11 and "dW1" not in so
+    # storage mode rounds exactly the bf16-stored tensors
+    frs = O.block8b_fwd_reparam(*args, store_bf16=True)
+    for k in ("h", "hg", "a", "out", "outg", "qkv"):
+        assert np.array_equal(frs[k], O.bf16_round(frs[k])), k
+    assert rel(frs["qkv"], fc["qkv"]) < 2e-2
 
 
 # ---------------------------------------------------------------- planted mistakes
