@@ -1,0 +1,117 @@
+"""Stage-isolated GPU parity at full size: each backward kernel is fed the
+oracle's own tensors (the rewritten form with the fused path's storage
+points) instead of the GPU's upstream outputs, so its result is compared
+with the oracle with no rounding cascade in between. These pin the
+statistics s and s' to the 1e-3 bound with a wide margin; the chained tests
+show what the whole bf16 pipeline gives.
+
+  * SwiGLU-backward GEMM + s (a7, a8), Llama-3-1B shape, all 8192 rows
+  * RMSNorm-backward GEMM + dgamma partials (a9, a11), same shape
+  * RoPE backward + s' (a12), Llama-3-8B shape, 64 sampled rows placed at
+    their positions in one 4096-row sequence (the map is row-independent)
+"""
+import numpy as np
+import pytest
+import torch
+
+from coda_inputs import WORKLOADS, mlp_block_inputs, block8b_inputs, positions
+from oracle import coda_oracle as O
+from tests._util import TOL_BF16, TOL_F32, assert_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def coda():
+    import __graft_entry__ as g
+    g.build()
+    import gemm_epilogue_fusion_tcgen05_gb300 as c
+    return c
+
+
+@pytest.fixture(scope="module")
+def oracle_1b():
+    sh = WORKLOADS["llama1b_mlp_bwd"]
+    inp = mlp_block_inputs(sh)
+    n = {k: O.to64(v) for k, v in inp.items()}
+    st = O.mlp_fwd_reparam(n["x"], n["z"], n["W0"], n["W1"], n["W2"], n["gamma"], store_bf16=True)
+    sb = O.mlp_bwd_reparam(st, n["x"], n["W0"], n["W1"], n["W2"], n["gamma"], n["dout"],
+                           store_bf16=True)
+    return sh, inp, st, sb
+
+
+def _t(a, dtype):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dtype).cuda()
+
+
+def test_swiglu_bwd_stage_full_size(coda, oracle_1b):
+    sh, inp, st, sb = oracle_1b
+    M, d, f = sh.M, sh.d, sh.f
+    y = _t(st["y"], torch.float32)
+    r = _t(st["r"], torch.float32)
+    dyhat = torch.empty((M, 2 * f), dtype=torch.bfloat16, device="cuda")
+    spart = torch.empty((coda.col_tiles(f), M), dtype=torch.float32, device="cuda")
+    s = torch.empty((M,), dtype=torch.float32, device="cuda")
+    coda.coda_gemm_rowscale_swiglu_bwd(inp["dout"].cuda(), inp["W2"].cuda(), y, r, dyhat, spart)
+    coda.coda_row_rms_bwd(spart, s, d)
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    assert_close("s (stage)", s, sb["s"], TOL_F32)
+    assert_close("dyhat (stage)", dyhat, sb["dyhat"], TOL_BF16)
+
+
+def test_norm_bwd_stage_full_size(coda, oracle_1b):
+    sh, inp, st, sb = oracle_1b
+    M, d, f = sh.M, sh.d, sh.f
+    dh = torch.empty((M, d), dtype=torch.bfloat16, device="cuda")
+    dgp = torch.empty((coda.row_tiles32(M), d), dtype=torch.float32, device="cuda")
+    dgamma = torch.empty((d,), dtype=torch.float32, device="cuda")
+    coda.coda_gemm_resid_norm_stats_bwd(_t(sb["dyhat"], torch.bfloat16), inp["W1"].cuda(),
+                                        _t(st["h"], torch.bfloat16), inp["gamma"].cuda(),
+                                        _t(st["r"], torch.float32), _t(sb["s"], torch.float32),
+                                        dh, dgp)
+    coda.coda_col_reduce(dgp, dgamma)
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    assert_close("dh (stage)", dh, sb["dh"], TOL_BF16)
+    assert_close("dgamma (stage)", dgamma, sb["dgamma"], 1e-3)
+
+
+def test_rope_bwd_stage_8b_shape(coda):
+    from gemm_epilogue_fusion_tcgen05_gb300 import blocks
+    sh = WORKLOADS["llama8b_block"]
+    inp = block8b_inputs(sh)
+    rng = np.random.default_rng(7)
+    rows = np.array(sorted(set(rng.choice(sh.M, 60, replace=False).tolist()) | {0, 4095, 4096, sh.M - 1}))
+    n = {k: O.to64(v[rows]) if v.dim() == 2 and v.shape[0] == sh.M else O.to64(v)
+         for k, v in inp.items()}
+    pos = positions(sh.M, sh.seq_len).numpy()[rows]
+    fr = O.block8b_fwd_reparam(n["o"], n["z"], n["Wo"], n["W1"], n["W2"], n["gamma2"], n["gamma1"],
+                               n["Wqkv"], pos, sh.n_rope_cols, sh.head_dim, sh.theta, store_bf16=True)
+    br = O.block8b_bwd_reparam(fr, n["o"], n["Wo"], n["W1"], n["W2"], n["gamma2"], n["gamma1"],
+                               n["Wqkv"], n["dqkv"], n["dres"], pos, sh.n_rope_cols, sh.head_dim,
+                               sh.theta, store_bf16=True, stat_only=True)
+    # one 4096-row sequence: row p holds the sampled token whose position is p
+    # (two samples with the same position would collide: keep the first)
+    L, N = sh.seq_len, sh.n_qkv
+    q = np.zeros((L, N))
+    dq = np.zeros((L, N))
+    r1 = np.ones(L)
+    keep = {}
+    for i, p in enumerate(pos):
+        keep.setdefault(int(p), i)
+    for p, i in keep.items():
+        q[p] = fr["qkv_save"][i]
+        dq[p] = n["dqkv"][i]
+        r1[p] = fr["r1"][i]
+    cs = blocks.rope_table(sh.seq_len, sh.head_dim, sh.theta, "cuda")
+    out = torch.empty((L, N), dtype=torch.bfloat16, device="cuda")
+    s1 = torch.empty((L,), dtype=torch.float32, device="cuda")
+    coda.coda_gemm_rope_bwd(_t(dq, torch.bfloat16), _t(q, torch.float32), _t(r1, torch.float32), cs,
+                            sh.seq_len, sh.head_dim, sh.n_rope_cols, out, s1, sh.d)
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    ps = np.array(sorted(keep))
+    idx = np.array([keep[p] for p in ps])
+    assert_close("s1 (stage)", s1.cpu()[ps], br["s1"][idx], TOL_F32)
+    assert_close("dqkv_hat (stage)", out.cpu()[ps], br["dqkv_hat"][idx], TOL_BF16)
