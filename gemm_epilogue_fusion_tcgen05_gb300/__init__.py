@@ -17,7 +17,7 @@ __all__ = [
     "coda_gemm_rowscale_swiglu", "coda_gemm_rope", "coda_rope_table", "coda_lmhead_ce",
     "coda_lmhead_ce_workspace_size", "coda_gemm_rowscale_swiglu_bwd", "coda_row_rms_bwd",
     "coda_gemm_resid_norm_stats_bwd", "coda_col_reduce", "coda_gemm_rope_bwd",
-    "coda_selftest_bounded_wait",
+    "coda_selftest_bounded_wait", "coda_lmhead_ce_noalloc",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoda.so")
@@ -50,6 +50,8 @@ EXPORTS = {
     "coda_col_reduce": (_I, [_P, _I, _I, _P, _P]),
     "coda_gemm_rope_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _P]),
     "coda_selftest_bounded_wait": (_I, [_I, _P]),
+    "coda_lmhead_ce_noalloc_capacity": (_Z, []),
+    "coda_lmhead_ce_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
 }
 
 
@@ -217,6 +219,21 @@ def coda_lmhead_ce(hidden, W, targets, lse, loss, ws, stream=None):
     _check(lib().coda_lmhead_ce(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(lse), _ptr(loss),
                                 _ptr(ws), ws.numel() * ws.element_size(), M, V, d,
                                 _stream(stream)))
+
+
+def coda_lmhead_ce_noalloc(hidden, W, targets, lse, loss, stream=None):
+    """coda_lmhead_ce with the library's own fixed scratch array instead of a
+    caller workspace, for callers that may not allocate device memory (see
+    include/coda.h for the row limit and the sharing rules)."""
+    M, d = hidden.shape
+    V = W.shape[1]
+    _req(hidden, bf16, "hidden")
+    _req(W, bf16, "W")
+    _req(targets, i32, "targets", 1)
+    _req(lse, f32, "lse", 1)
+    _req(loss, f32, "loss", 1)
+    _check(lib().coda_lmhead_ce_noalloc(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(lse),
+                                        _ptr(loss), M, V, d, _stream(stream)))
 
 
 # ---------------------------------------------------------------- backward

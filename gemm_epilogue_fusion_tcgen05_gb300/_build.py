@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcoda.so")
 
 SOURCES = ["api.cu", "aux_kernels.cu", "gemm_plain.cu", "gemm_plain_t.cu", "gemm_fwd.cu",
-           "gemm_bwd.cu"]
+           "gemm_bwd.cu", "lmhead_noalloc.cu"]
 HEADERS = ["internal.h", "core/ptx.cuh", "core/gemm.cuh", "core/gemm2.cuh", "core/epilogues.cuh", "core/launch.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

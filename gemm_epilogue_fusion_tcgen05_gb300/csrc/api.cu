@@ -171,6 +171,11 @@ constexpr int kMaxDim = 1 << 30;
 
 }  // namespace
 
+namespace coda {
+// lets other translation units of the library report a host-side error
+void set_last_error(const char* msg) { t_last_error = msg; }
+}  // namespace coda
+
 extern "C" {
 
 int coda_version(void) { return 100; }

@@ -80,6 +80,9 @@ struct NormBwdArgs {
 };
 cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc);
 
+// text returned by coda_last_error_string() for this thread
+void set_last_error(const char* msg);
+
 // tile width of every GEMM in the library (columns per accumulator tile)
 constexpr int kTileN = 256;
 constexpr int kTileM = 128;

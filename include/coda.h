@@ -169,6 +169,30 @@ coda_status_t coda_lmhead_ce(const void* hidden, const void* W, const int32_t* t
                              float* loss, void* ws, size_t ws_bytes, int M, int V, int d,
                              coda_stream_t stream);
 
+/* LM head + cross-entropy without any scratch from the caller (the pages
+ * have no counterpart: this is a convenience of this library). Same inputs,
+ * outputs and results as coda_lmhead_ce; the scratch comes from an array of
+ * coda_lmhead_ce_noalloc_capacity() bytes (16 MiB) that the library keeps in
+ * the memory of every GPU that loads it, until the process exits.
+ * For callers that may not allocate device memory: e.g. an operator hook
+ * that receives only its inputs and outputs while a host framework's
+ * allocator owns the rest of the device, or a loop where cudaMalloc /
+ * cudaFree (which can synchronise the device) are not allowed.
+ *   - M and V must satisfy coda_lmhead_ce_workspace_size(M, V) <=
+ *     coda_lmhead_ce_noalloc_capacity() (about 4100 rows at V = 128256);
+ *     larger requests return CODA_ERR_INVALID_VALUE with an explanation.
+ *   - The first call on each device looks the array's device address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array: calls whose work overlaps on the GPU (e.g.
+ *     on two streams at once) race and give wrong results. Each call
+ *     rewrites every entry it reads, so no clearing is needed.
+ *   - Allocates nothing (no cudaMalloc, cudaFree or allocating library call). */
+size_t coda_lmhead_ce_noalloc_capacity(void);
+coda_status_t coda_lmhead_ce_noalloc(const void* hidden, const void* W, const int32_t* targets,
+                                     float* lse, float* loss, int M, int V, int d,
+                                     coda_stream_t stream);
+
 /* ------------------------------------------------------------ backward */
 
 /* Reverse-fused SwiGLU backward ([notes] s3 "Reverse Fusion": f'(h)
