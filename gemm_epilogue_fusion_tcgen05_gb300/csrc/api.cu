@@ -407,7 +407,7 @@ coda_status_t coda_gemm_rowscale_swiglu_bwd(const void* dout, const void* W2, co
   CHECK_MAP(map_a(&p.tmA, dout, d, 0, M, d));
   CHECK_MAP(map_b(&p.tmB, W2, d, 1, f, d));  // B[k, n] = W2[n, k]
   CHECK_MAP(map_f32_32(&p.tm_y, y, M, 2 * f, 2 * f));
-  CHECK_MAP(map_bf16_64(&p.tm_dy, dyhat, M, 2 * f, 2 * f));
+  CHECK_MAP(map_bf16_32(&p.tm_dy, dyhat, M, 2 * f, 2 * f));
   p.r = r;
   p.spart = spart;
   p.M = M;

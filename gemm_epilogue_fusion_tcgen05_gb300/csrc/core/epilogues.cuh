@@ -10,8 +10,10 @@
 // Each epilogue warp owns 32 rows of the 128 x BN accumulator tile (its TMEM
 // lane quarter) and walks the tile in chunks of 32 accumulator columns:
 // tcgen05.ld -> math -> st.shared into a swizzled box -> one TMA store per
-// output. Tile loads for the next chunk are issued before the current chunk
-// is computed (double-buffered staging).
+// output. Staging buffers come in sets used round-robin, one chunk each: a
+// chunk waits only for the stores of chunks two or more back (never for the
+// previous chunk's), and epilogues with tile loads keep three sets so the
+// load for chunk c+1 is in flight while chunk c is computed.
 #pragma once
 #include "gemm.cuh"
 
@@ -79,12 +81,15 @@ __device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
 // ------------------------------------------------------------------ plain
 // C = acc (+ resid), optional per-row sum of squares of the stored value's
 // fp32 pre-image. fp32 output rows are 128 bytes per 32 columns, bf16 64.
+// Staging sets: 2 (store only) or 3 (the residual box of chunk c+1 is loaded
+// while chunk c is computed).
 template <bool OUT_F32, bool RESID, bool ROWSQ>
 struct EpiPlain {
   static_assert(!(OUT_F32 && RESID), "residual is defined for bf16 outputs");
   static constexpr int kRowB = OUT_F32 ? 128 : 64;
   static constexpr int kBufB = 32 * kRowB;
-  static constexpr int kSmemPerWarp = 2 * kBufB;
+  static constexpr int kSets = RESID ? 3 : 2;
+  static constexpr int kSmemPerWarp = kSets * kBufB;
   struct Params {
     CUtensorMap tm_c;
     CUtensorMap tm_r;
@@ -94,8 +99,8 @@ struct EpiPlain {
   static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
                                                   int m0, int n0) {
     if constexpr (RESID) {
-      c.stores_read_done();
-      const int b = c.cnt & 1;
+      c.stores_read_but_last();
+      const int b = c.cnt % kSets;
       c.load(&p.tm_r, b, c.buf + b * kBufB, n0, m0 + 32 * c.q, kBufB);
     }
   }
@@ -105,12 +110,13 @@ struct EpiPlain {
     constexpr int NCH = BN / 32;
     float ss = 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
-      const int b = c.cnt & 1;
+      const int b = c.cnt % kSets;
       const uint32_t buf = c.buf + b * kBufB;
-      c.stores_read_done();
+      c.stores_read_but_last();
       if constexpr (RESID) {
+        const int nbf = (c.cnt + 1) % kSets;
         if (ch + 1 < NCH)
-          c.load(&p.tm_r, b ^ 1, c.buf + (b ^ 1) * kBufB, n0 + (ch + 1) * 32, m0 + 32 * c.q, kBufB);
+          c.load(&p.tm_r, nbf, c.buf + nbf * kBufB, n0 + (ch + 1) * 32, m0 + 32 * c.q, kBufB);
       }
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
@@ -155,9 +161,13 @@ struct EpiPlain {
 // "Kernel Example": residual D = acc + C, block sum of squares of the
 // unscaled D, side output D * gamma[n]):
 //   h = acc + z (stored), hg = h * gamma (stored), part[nb, m] = sum_n h^2
+// Three staging sets of {H (z in, h out), G}: the z box of chunk c+1 loads
+// while chunk c is computed and the stores of chunk c-1 drain.
 struct EpiResidNormStats {
   static constexpr int kBufB = 2048;  // 32 rows x 32 bf16
-  static constexpr int kSmemPerWarp = 4 * kBufB;  // H[2] (z in, h out) + G[2]
+  static constexpr int kSets = 3;
+  static constexpr int kSetB = 2 * kBufB;
+  static constexpr int kSmemPerWarp = kSets * kSetB;
   struct Params {
     CUtensorMap tm_z, tm_h, tm_hg;
     const __nv_bfloat16* gamma;
@@ -166,9 +176,9 @@ struct EpiResidNormStats {
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
                                                   int m0, int n0) {
-    c.stores_read_done();
-    const int b = c.cnt & 1;
-    c.load(&p.tm_z, b, c.buf + b * kBufB, n0, m0 + 32 * c.q, kBufB);
+    c.stores_read_but_last();
+    const int b = c.cnt % kSets;
+    c.load(&p.tm_z, b, c.buf + b * kSetB, n0, m0 + 32 * c.q, kBufB);
   }
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
@@ -176,12 +186,14 @@ struct EpiResidNormStats {
     constexpr int NCH = BN / 32;
     float ss = 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
-      const int b = c.cnt & 1;
-      const uint32_t hbuf = c.buf + b * kBufB;
-      const uint32_t gbuf = c.buf + (2 + b) * kBufB;
-      c.stores_read_done();
-      if (ch + 1 < NCH)
-        c.load(&p.tm_z, b ^ 1, c.buf + (b ^ 1) * kBufB, n0 + (ch + 1) * 32, m0 + 32 * c.q, kBufB);
+      const int b = c.cnt % kSets;
+      const uint32_t hbuf = c.buf + b * kSetB;
+      const uint32_t gbuf = hbuf + kBufB;
+      c.stores_read_but_last();
+      if (ch + 1 < NCH) {
+        const int nbf = (c.cnt + 1) % kSets;
+        c.load(&p.tm_z, nbf, c.buf + nbf * kSetB, n0 + (ch + 1) * 32, m0 + 32 * c.q, kBufB);
+      }
       float v[32], gm[32], z[32];
       tmem_ld32(taddr + ch * 32, v);
       load_nvec32(p.gamma, n0 + ch * 32, g.N, gm);
@@ -220,7 +232,8 @@ struct EpiResidNormStats {
 struct EpiRowScaleSwiGLU {
   static constexpr int kABufB = 1024;  // 32 rows x 16 bf16 (32-byte rows)
   static constexpr int kYBufB = 4096;  // 32 rows x 32 fp32 (128-byte rows)
-  static constexpr int kSmemPerWarp = 2 * kABufB + 2 * kYBufB;
+  static constexpr int kSetB = kABufB + kYBufB;
+  static constexpr int kSmemPerWarp = 2 * kSetB;
   struct Params {
     CUtensorMap tm_a, tm_y;
     const float* r;
@@ -236,9 +249,9 @@ struct EpiRowScaleSwiGLU {
     const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
       const int b = c.cnt & 1;
-      const uint32_t abuf = c.buf + b * kABufB;
-      const uint32_t ybuf = c.buf + 2 * kABufB + b * kYBufB;
-      c.stores_read_done();
+      const uint32_t abuf = c.buf + b * kSetB;
+      const uint32_t ybuf = abuf + kABufB;
+      c.stores_read_but_last();
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
       uint32_t ap[8];
@@ -284,7 +297,8 @@ struct EpiRowScaleSwiGLU {
 struct EpiRope {
   static constexpr int kBufB = 2048;   // 32 rows x 32 bf16
   static constexpr int kSBufB = 4096;  // 32 rows x 32 fp32
-  static constexpr int kSmemPerWarp = 2 * kBufB + 2 * kSBufB;
+  static constexpr int kSetB = kBufB + kSBufB;
+  static constexpr int kSmemPerWarp = 2 * kSetB;
   struct Params {
     CUtensorMap tm_out, tm_save;
     const float* r;        // nullable: no row scale
@@ -303,9 +317,9 @@ struct EpiRope {
     const float4* csrow = reinterpret_cast<const float4*>(p.cs + (size_t)pos * (p.head_dim / 2));
     for (int ch = 0; ch < NCH; ++ch) {
       const int b = c.cnt & 1;
-      const uint32_t buf = c.buf + b * kBufB;
-      const uint32_t sbuf = c.buf + 2 * kBufB + b * kSBufB;
-      c.stores_read_done();
+      const uint32_t buf = c.buf + b * kSetB;
+      const uint32_t sbuf = buf + kBufB;
+      c.stores_read_but_last();
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
       const int col0 = n0 + ch * 32;
@@ -409,54 +423,49 @@ struct EpiCE {
 //   da = acc ; (g, u) = saved y pair (fp32) ; sg = sigmoid(g)
 //   dg = da u sg (1 + g (1 - sg)) ; du = da g sg
 //   spart[nb, m] = sum (dg g + du u) ; dyhat = r (dg, du) (bf16)
-// Per 32-column chunk of da: two fp32 boxes of y (64 columns) in, one bf16
-// box of dyhat (64 columns) out.
+// Per 16-column chunk of da: one fp32 box of y (32 columns) in, one bf16 box
+// of dyhat (32 columns) out; three staging sets.
 struct EpiSwiGLUBwd {
-  static constexpr int kYBufB = 8192;   // 2 boxes of 32 rows x 32 fp32
-  static constexpr int kOBufB = 4096;   // 32 rows x 64 bf16
+  static constexpr int kYBufB = 4096;   // 32 rows x 32 fp32
+  static constexpr int kOBufB = 2048;   // 32 rows x 32 bf16
+  static constexpr int kSets = 3;
   static constexpr int kSetB = kYBufB + kOBufB;
-  static constexpr int kSmemPerWarp = 2 * kSetB;
+  static constexpr int kSmemPerWarp = kSets * kSetB;
   struct Params {
     CUtensorMap tm_y, tm_dy;
     const float* r;
     float* spart;  // [tiles_n, M]
   };
-  static __device__ __forceinline__ void load_y(const Params& p, EpiCtx& c, int b, int col0, int m0) {
-    const uint32_t ybuf = c.buf + b * kSetB;
-    if (c.lane == 0) {
-      mbar_arrive_expect_tx(c.bar(b), kYBufB);
-      tma_load_2d(&p.tm_y, ybuf, c.bar(b), col0, m0 + 32 * c.q);
-      tma_load_2d(&p.tm_y, ybuf + 4096, c.bar(b), col0 + 32, m0 + 32 * c.q);
-    }
-    c.pending |= 1u << b;
-  }
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
                                                   int m0, int n0) {
-    c.stores_read_done();
-    load_y(p, c, c.cnt & 1, 2 * n0, m0);
+    c.stores_read_but_last();
+    const int b = c.cnt % kSets;
+    c.load(&p.tm_y, b, c.buf + b * kSetB, 2 * n0, m0 + 32 * c.q, kYBufB);
   }
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
                                               int n0, int nb, uint32_t taddr) {
-    constexpr int NCH = BN / 32;
+    constexpr int NCH = BN / 16;
     const int row = m0 + 32 * c.q + c.lane;
     const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
     float ss = 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
-      const int b = c.cnt & 1;
+      const int b = c.cnt % kSets;
       const uint32_t ybuf = c.buf + b * kSetB;
       const uint32_t obuf = ybuf + kYBufB;
-      c.stores_read_done();
-      if (ch + 1 < NCH) load_y(p, c, b ^ 1, 2 * (n0 + (ch + 1) * 32), m0);
-      float da[32];
-      tmem_ld32(taddr + ch * 32, da);
+      c.stores_read_but_last();
+      if (ch + 1 < NCH) {
+        const int nbf = (c.cnt + 1) % kSets;
+        c.load(&p.tm_y, nbf, c.buf + nbf * kSetB, 2 * (n0 + (ch + 1) * 16), m0 + 32 * c.q, kYBufB);
+      }
+      float da[16];
+      tmem_ld16(taddr + ch * 16, da);
       if (!c.wait(b, 12)) return false;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {  // output chunk k = pairs 4k .. 4k+3
-        const uint32_t yb = ybuf + (k >> 2) * 4096;
-        const uint4 y0 = ld_shared_v4(yb + swz<128>(c.lane, 2 * (k & 3)));
-        const uint4 y1 = ld_shared_v4(yb + swz<128>(c.lane, 2 * (k & 3) + 1));
+      for (int k = 0; k < 4; ++k) {  // output chunk k = pairs 4k .. 4k+3
+        const uint4 y0 = ld_shared_v4(ybuf + swz<128>(c.lane, 2 * k));
+        const uint4 y1 = ld_shared_v4(ybuf + swz<128>(c.lane, 2 * k + 1));
         const float gy[4] = {__uint_as_float(y0.x), __uint_as_float(y0.z), __uint_as_float(y1.x),
                              __uint_as_float(y1.z)};
         const float uy[4] = {__uint_as_float(y0.y), __uint_as_float(y0.w), __uint_as_float(y1.y),
@@ -472,12 +481,12 @@ struct EpiSwiGLUBwd {
           ss = fmaf(dg, gg, fmaf(du, uu, ss));
           outw[t] = pack_bf16(rr * dg, rr * du);
         }
-        st_shared_v4(obuf + swz<128>(c.lane, k), outw[0], outw[1], outw[2], outw[3]);
+        st_shared_v4(obuf + swz<64>(c.lane, k), outw[0], outw[1], outw[2], outw[3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
-        tma_store_2d(&p.tm_dy, obuf, 2 * (n0 + ch * 32), m0 + 32 * c.q);
+        tma_store_2d(&p.tm_dy, obuf, 2 * (n0 + ch * 16), m0 + 32 * c.q);
         bulk_commit();
       }
       ++c.cnt;
@@ -492,9 +501,12 @@ struct EpiSwiGLUBwd {
 // CODA", s3): P = r dh2, so
 //   dh = gamma P - r^2 s h (+ dres) (stored) ; dgamma partial = sum_rows P h
 // The column sums use a warp transpose-reduce; partials are per 32 rows.
+// Three staging sets of {H (h in, dh out), R (dres)}.
 struct EpiNormBwd {
   static constexpr int kBufB = 2048;
-  static constexpr int kSmemPerWarp = 4 * kBufB;  // H[2] (h in, dh out), R[2] (dres)
+  static constexpr int kSets = 3;
+  static constexpr int kSetB = 2 * kBufB;
+  static constexpr int kSmemPerWarp = kSets * kSetB;
   struct Params {
     CUtensorMap tm_h, tm_dres, tm_dh;
     const __nv_bfloat16* gamma;
@@ -503,13 +515,16 @@ struct EpiNormBwd {
     float* dgpart;  // [ceil(M/32), N]
     int has_dres;
   };
+  static __device__ __forceinline__ void load_set(const Params& p, EpiCtx& c, int b, int n, int m0) {
+    const uint32_t base = c.buf + b * kSetB;
+    c.load(&p.tm_h, b, base, n, m0 + 32 * c.q, kBufB);
+    if (p.has_dres) c.load(&p.tm_dres, kSets + b, base + kBufB, n, m0 + 32 * c.q, kBufB);
+  }
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
                                                   int m0, int n0) {
-    c.stores_read_done();
-    const int b = c.cnt & 1;
-    c.load(&p.tm_h, b, c.buf + b * kBufB, n0, m0 + 32 * c.q, kBufB);
-    if (p.has_dres) c.load(&p.tm_dres, 2 + b, c.buf + (2 + b) * kBufB, n0, m0 + 32 * c.q, kBufB);
+    c.stores_read_but_last();
+    load_set(p, c, c.cnt % kSets, n0, m0);
   }
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
@@ -521,15 +536,11 @@ struct EpiNormBwd {
     const float k2 = rr * rr * ss;
     const int prow = (m0 >> 5) + c.q;  // partial row (32 rows each)
     for (int ch = 0; ch < NCH; ++ch) {
-      const int b = c.cnt & 1;
-      const uint32_t hbuf = c.buf + b * kBufB;
-      const uint32_t rbuf = c.buf + (2 + b) * kBufB;
-      c.stores_read_done();
-      if (ch + 1 < NCH) {
-        const int nn = n0 + (ch + 1) * 32;
-        c.load(&p.tm_h, b ^ 1, c.buf + (b ^ 1) * kBufB, nn, m0 + 32 * c.q, kBufB);
-        if (p.has_dres) c.load(&p.tm_dres, 2 + (b ^ 1), c.buf + (2 + (b ^ 1)) * kBufB, nn, m0 + 32 * c.q, kBufB);
-      }
+      const int b = c.cnt % kSets;
+      const uint32_t hbuf = c.buf + b * kSetB;
+      const uint32_t rbuf = hbuf + kBufB;
+      c.stores_read_but_last();
+      if (ch + 1 < NCH) load_set(p, c, (c.cnt + 1) % kSets, n0 + (ch + 1) * 32, m0);
       float P[32], h[32], gm[32];
       tmem_ld32(taddr + ch * 32, P);
       load_nvec32(p.gamma, n0 + ch * 32, g.N, gm);
@@ -539,7 +550,7 @@ struct EpiNormBwd {
 #pragma unroll
       for (int j = 0; j < 32; ++j) dh[j] = gm[j] * P[j] - k2 * h[j];
       if (p.has_dres) {
-        if (!c.wait(2 + b, 14)) return false;
+        if (!c.wait(kSets + b, 14)) return false;
         float rz[32];
         read_bf16x32(rbuf, c.lane, rz);
 #pragma unroll

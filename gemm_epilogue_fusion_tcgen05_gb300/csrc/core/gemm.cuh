@@ -28,6 +28,7 @@ constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle ro
 constexpr int kUK = 16;         // K per tcgen05.mma (kind::f16)
 constexpr int kSmemMax = 232448;
 constexpr int kEpiWarps = 4;
+constexpr int kEpiBars = 8;     // mbarriers per epilogue warp (tile loads)
 
 struct GemmArgs {
   int M, N, K;
@@ -41,10 +42,10 @@ struct GemmArgs {
 // epilogue tile loads, their phase bits, and a running chunk counter.
 struct EpiCtx {
   uint32_t buf;      // shared address of this warp's staging area
-  uint32_t bar0;     // first of this warp's 4 mbarriers (8 bytes apart)
+  uint32_t bar0;     // first of this warp's kEpiBars mbarriers (8 bytes apart)
   uint32_t phase;    // parity bit per barrier
   uint32_t pending;  // barriers with a load issued and not yet waited on
-  uint32_t cnt;      // chunks processed so far (selects the double buffer)
+  uint32_t cnt;      // chunks processed so far (selects the staging set)
   int lane, q;       // lane; TMEM lane quarter = row block of 32 inside the tile
   DevError e;
 
@@ -67,13 +68,19 @@ struct EpiCtx {
     return ok;
   }
   __device__ __forceinline__ void drain() {
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < kEpiBars; ++j)
       if (pending & (1u << j)) mbar_drain(bar(j), (phase >> j) & 1u, 50000000ull);
     pending = 0;
   }
   // lane 0 makes sure every earlier TMA store has finished reading its smem
   __device__ __forceinline__ void stores_read_done() {
     if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+  }
+  // ... every earlier store except the most recent group (the previous
+  // chunk's): enough before reusing a staging set two chunks later
+  __device__ __forceinline__ void stores_read_but_last() {
+    if (lane == 0) bulk_wait_read<1>();
     __syncwarp();
   }
 };
@@ -130,9 +137,9 @@ __global__ void __launch_bounds__(T::kThreads, 1)
   auto empty = [&](int s) { return bars + 8u * (S + s); };
   auto tfull = [&](int i) { return bars + 8u * (2 * S + i); };
   auto tempty = [&](int i) { return bars + 8u * (2 * S + 2 + i); };
-  const uint32_t epibar = bars + 8u * (2 * S + 4);      // 4 warps x 4 barriers
-  const uint32_t drainbar = bars + 8u * (2 * S + 20);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(barp + 8 * (2 * S + 21));
+  const uint32_t epibar = bars + 8u * (2 * S + 4);      // 4 warps x kEpiBars barriers
+  const uint32_t drainbar = bars + 8u * (2 * S + 4 + kEpiBars * kEpiWarps);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(barp + 8 * (2 * S + 5 + kEpiBars * kEpiWarps));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -147,7 +154,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
       mbar_init(tfull(i), 1);
       mbar_init(tempty(i), kEpiWarps);
     }
-    for (int j = 0; j < 4 * kEpiWarps; ++j) mbar_init(epibar + 8u * j, 1);
+    for (int j = 0; j < kEpiBars * kEpiWarps; ++j) mbar_init(epibar + 8u * j, 1);
     mbar_init(drainbar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     const int ew = warp - 2;
     EpiCtx ctx;
     ctx.buf = sEpi + ew * T::Epi::kSmemPerWarp;
-    ctx.bar0 = epibar + 8u * 4 * ew;
+    ctx.bar0 = epibar + 8u * kEpiBars * ew;
     ctx.phase = 0;
     ctx.pending = 0;
     ctx.cnt = 0;

@@ -63,9 +63,9 @@ __global__ void __launch_bounds__(T::kThreads, 1)
   auto empty = [&](int s) { return bars + 8u * (S + s); };
   auto tfull = [&](int i) { return bars + 8u * (2 * S + i); };
   auto tempty = [&](int i) { return bars + 8u * (2 * S + 2 + i); };
-  const uint32_t epibar = bars + 8u * (2 * S + 4);
-  const uint32_t drainbar = bars + 8u * (2 * S + 20);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(barp + 8 * (2 * S + 21));
+  const uint32_t epibar = bars + 8u * (2 * S + 4);      // 4 warps x kEpiBars barriers
+  const uint32_t drainbar = bars + 8u * (2 * S + 4 + kEpiBars * kEpiWarps);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(barp + 8 * (2 * S + 5 + kEpiBars * kEpiWarps));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
       mbar_init(tfull(i), 1);
       mbar_init(tempty(i), 2 * kEpiWarps);
     }
-    for (int j = 0; j < 4 * kEpiWarps; ++j) mbar_init(epibar + 8u * j, 1);
+    for (int j = 0; j < kEpiBars * kEpiWarps; ++j) mbar_init(epibar + 8u * j, 1);
     mbar_init(drainbar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     const int ew = warp - 2;
     EpiCtx ctx;
     ctx.buf = sEpi + ew * T::Epi::kSmemPerWarp;
-    ctx.bar0 = epibar + 8u * 4 * ew;
+    ctx.bar0 = epibar + 8u * kEpiBars * ew;
     ctx.phase = 0;
     ctx.pending = 0;
     ctx.cnt = 0;
