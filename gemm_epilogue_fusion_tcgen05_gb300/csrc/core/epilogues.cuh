@@ -10,10 +10,9 @@
 // Each epilogue warp owns 32 rows of the 128 x BN accumulator tile (its TMEM
 // lane quarter) and walks the tile in chunks of 32 accumulator columns:
 // tcgen05.ld -> math -> st.shared into a swizzled box -> one TMA store per
-// output. Staging buffers come in sets used round-robin, one chunk each: a
-// chunk waits only for the stores of chunks two or more back (never for the
-// previous chunk's), and epilogues with tile loads keep three sets so the
-// load for chunk c+1 is in flight while chunk c is computed.
+// output. Store staging alternates between two sets, so a chunk waits only
+// for the stores of chunks two or more back; epilogues with tile loads keep a
+// separate ring of load slots and issue each box several chunks ahead.
 #pragma once
 #include "gemm.cuh"
 
@@ -81,27 +80,31 @@ __device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
 // ------------------------------------------------------------------ plain
 // C = acc (+ resid), optional per-row sum of squares of the stored value's
 // fp32 pre-image. fp32 output rows are 128 bytes per 32 columns, bf16 64.
-// Staging sets: 2 (store only) or 3 (the residual box of chunk c+1 is loaded
-// while chunk c is computed).
+// Two store sets; with a residual, a ring of kNL load slots keeps the
+// residual boxes of the next kNL-1 chunks in flight.
 template <bool OUT_F32, bool RESID, bool ROWSQ>
 struct EpiPlain {
   static_assert(!(OUT_F32 && RESID), "residual is defined for bf16 outputs");
   static constexpr int kRowB = OUT_F32 ? 128 : 64;
   static constexpr int kBufB = 32 * kRowB;
-  static constexpr int kSets = RESID ? 3 : 2;
-  static constexpr int kSmemPerWarp = kSets * kBufB;
+  static constexpr int kNL = RESID ? 4 : 0;  // load slots (32 rows x 32 bf16 each)
+  static constexpr int kLoadB = 2048;
+  static constexpr int kSmemPerWarp = kNL * kLoadB + 2 * kBufB;
   struct Params {
     CUtensorMap tm_c;
     CUtensorMap tm_r;
     float* rowsq;  // [tiles_n, M] when ROWSQ
   };
+  static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int n,
+                                               int m0) {
+    const int slot = k % kNL;
+    c.load(&p.tm_r, slot, c.buf + slot * kLoadB, n, m0 + 32 * c.q, kLoadB);
+  }
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
                                                   int m0, int n0) {
     if constexpr (RESID) {
-      c.stores_read_but_last();
-      const int b = c.cnt % kSets;
-      c.load(&p.tm_r, b, c.buf + b * kBufB, n0, m0 + 32 * c.q, kBufB);
+      for (int i = 0; i < kNL - 1; ++i) issue(p, c, c.cnt + i, n0 + i * 32, m0);
     }
   }
   template <int BN>
@@ -110,20 +113,18 @@ struct EpiPlain {
     constexpr int NCH = BN / 32;
     float ss = 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
-      const int b = c.cnt % kSets;
-      const uint32_t buf = c.buf + b * kBufB;
+      const uint32_t buf = c.buf + kNL * kLoadB + (c.cnt & 1) * kBufB;
       c.stores_read_but_last();
       if constexpr (RESID) {
-        const int nbf = (c.cnt + 1) % kSets;
-        if (ch + 1 < NCH)
-          c.load(&p.tm_r, nbf, c.buf + nbf * kBufB, n0 + (ch + 1) * 32, m0 + 32 * c.q, kBufB);
+        if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, n0 + (ch + kNL - 1) * 32, m0);
       }
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
       if constexpr (RESID) {
-        if (!c.wait(b, 10)) return false;
+        const int slot = c.cnt % kNL;
+        if (!c.wait(slot, 10)) return false;
         float z[32];
-        read_bf16x32(buf, c.lane, z);
+        read_bf16x32(c.buf + slot * kLoadB, c.lane, z);
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] += z[j];
       }
@@ -161,24 +162,27 @@ struct EpiPlain {
 // "Kernel Example": residual D = acc + C, block sum of squares of the
 // unscaled D, side output D * gamma[n]):
 //   h = acc + z (stored), hg = h * gamma (stored), part[nb, m] = sum_n h^2
-// Three staging sets of {H (z in, h out), G}: the z box of chunk c+1 loads
-// while chunk c is computed and the stores of chunk c-1 drain.
+// A ring of kNL load slots keeps the z boxes of the next kNL-1 chunks in
+// flight; two store sets of {h, hg}.
 struct EpiResidNormStats {
   static constexpr int kBufB = 2048;  // 32 rows x 32 bf16
-  static constexpr int kSets = 3;
-  static constexpr int kSetB = 2 * kBufB;
-  static constexpr int kSmemPerWarp = kSets * kSetB;
+  static constexpr int kNL = 4;
+  static constexpr int kStoreB = 2 * kBufB;
+  static constexpr int kSmemPerWarp = kNL * kBufB + 2 * kStoreB;
   struct Params {
     CUtensorMap tm_z, tm_h, tm_hg;
     const __nv_bfloat16* gamma;
     float* part;  // [tiles_n, M]
   };
+  static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int n,
+                                               int m0) {
+    const int slot = k % kNL;
+    c.load(&p.tm_z, slot, c.buf + slot * kBufB, n, m0 + 32 * c.q, kBufB);
+  }
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
                                                   int m0, int n0) {
-    c.stores_read_but_last();
-    const int b = c.cnt % kSets;
-    c.load(&p.tm_z, b, c.buf + b * kSetB, n0, m0 + 32 * c.q, kBufB);
+    for (int i = 0; i < kNL - 1; ++i) issue(p, c, c.cnt + i, n0 + i * 32, m0);
   }
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
@@ -186,19 +190,16 @@ struct EpiResidNormStats {
     constexpr int NCH = BN / 32;
     float ss = 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
-      const int b = c.cnt % kSets;
-      const uint32_t hbuf = c.buf + b * kSetB;
+      const int slot = c.cnt % kNL;
+      const uint32_t hbuf = c.buf + kNL * kBufB + (c.cnt & 1) * kStoreB;
       const uint32_t gbuf = hbuf + kBufB;
       c.stores_read_but_last();
-      if (ch + 1 < NCH) {
-        const int nbf = (c.cnt + 1) % kSets;
-        c.load(&p.tm_z, nbf, c.buf + nbf * kSetB, n0 + (ch + 1) * 32, m0 + 32 * c.q, kBufB);
-      }
+      if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, n0 + (ch + kNL - 1) * 32, m0);
       float v[32], gm[32], z[32];
       tmem_ld32(taddr + ch * 32, v);
       load_nvec32(p.gamma, n0 + ch * 32, g.N, gm);
-      if (!c.wait(b, 11)) return false;
-      read_bf16x32(hbuf, c.lane, z);
+      if (!c.wait(slot, 11)) return false;
+      read_bf16x32(c.buf + slot * kBufB, c.lane, z);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         v[j] += z[j];
@@ -424,24 +425,28 @@ struct EpiCE {
 //   dg = da u sg (1 + g (1 - sg)) ; du = da g sg
 //   spart[nb, m] = sum (dg g + du u) ; dyhat = r (dg, du) (bf16)
 // Per 16-column chunk of da: one fp32 box of y (32 columns) in, one bf16 box
-// of dyhat (32 columns) out; three staging sets.
+// of dyhat (32 columns) out. A ring of kNL load slots keeps the y boxes of
+// the next kNL-1 chunks in flight (this epilogue reads 4 bytes of y per
+// MMA column, so its loads must run far ahead); two store sets.
 struct EpiSwiGLUBwd {
   static constexpr int kYBufB = 4096;   // 32 rows x 32 fp32
   static constexpr int kOBufB = 2048;   // 32 rows x 32 bf16
-  static constexpr int kSets = 3;
-  static constexpr int kSetB = kYBufB + kOBufB;
-  static constexpr int kSmemPerWarp = kSets * kSetB;
+  static constexpr int kNL = 5;
+  static constexpr int kSmemPerWarp = kNL * kYBufB + 2 * kOBufB;
   struct Params {
     CUtensorMap tm_y, tm_dy;
     const float* r;
     float* spart;  // [tiles_n, M]
   };
+  static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int ycol,
+                                               int m0) {
+    const int slot = k % kNL;
+    c.load(&p.tm_y, slot, c.buf + slot * kYBufB, ycol, m0 + 32 * c.q, kYBufB);
+  }
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
                                                   int m0, int n0) {
-    c.stores_read_but_last();
-    const int b = c.cnt % kSets;
-    c.load(&p.tm_y, b, c.buf + b * kSetB, 2 * n0, m0 + 32 * c.q, kYBufB);
+    for (int i = 0; i < kNL - 1; ++i) issue(p, c, c.cnt + i, 2 * (n0 + i * 16), m0);
   }
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
@@ -451,17 +456,14 @@ struct EpiSwiGLUBwd {
     const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
     float ss = 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
-      const int b = c.cnt % kSets;
-      const uint32_t ybuf = c.buf + b * kSetB;
-      const uint32_t obuf = ybuf + kYBufB;
+      const int slot = c.cnt % kNL;
+      const uint32_t ybuf = c.buf + slot * kYBufB;
+      const uint32_t obuf = c.buf + kNL * kYBufB + (c.cnt & 1) * kOBufB;
       c.stores_read_but_last();
-      if (ch + 1 < NCH) {
-        const int nbf = (c.cnt + 1) % kSets;
-        c.load(&p.tm_y, nbf, c.buf + nbf * kSetB, 2 * (n0 + (ch + 1) * 16), m0 + 32 * c.q, kYBufB);
-      }
+      if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, 2 * (n0 + (ch + kNL - 1) * 16), m0);
       float da[16];
       tmem_ld16(taddr + ch * 16, da);
-      if (!c.wait(b, 12)) return false;
+      if (!c.wait(slot, 12)) return false;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {  // output chunk k = pairs 4k .. 4k+3
         const uint4 y0 = ld_shared_v4(ybuf + swz<128>(c.lane, 2 * k));
@@ -501,12 +503,13 @@ struct EpiSwiGLUBwd {
 // CODA", s3): P = r dh2, so
 //   dh = gamma P - r^2 s h (+ dres) (stored) ; dgamma partial = sum_rows P h
 // The column sums use a warp transpose-reduce; partials are per 32 rows.
-// Three staging sets of {H (h in, dh out), R (dres)}.
+// A ring of kNL load slots of {h, dres} boxes runs kNL-1 chunks ahead; two
+// store sets of dh.
 struct EpiNormBwd {
   static constexpr int kBufB = 2048;
-  static constexpr int kSets = 3;
-  static constexpr int kSetB = 2 * kBufB;
-  static constexpr int kSmemPerWarp = kSets * kSetB;
+  static constexpr int kNL = 4;
+  static constexpr int kLoadB = 2 * kBufB;
+  static constexpr int kSmemPerWarp = kNL * kLoadB + 2 * kBufB;
   struct Params {
     CUtensorMap tm_h, tm_dres, tm_dh;
     const __nv_bfloat16* gamma;
@@ -515,16 +518,17 @@ struct EpiNormBwd {
     float* dgpart;  // [ceil(M/32), N]
     int has_dres;
   };
-  static __device__ __forceinline__ void load_set(const Params& p, EpiCtx& c, int b, int n, int m0) {
-    const uint32_t base = c.buf + b * kSetB;
-    c.load(&p.tm_h, b, base, n, m0 + 32 * c.q, kBufB);
-    if (p.has_dres) c.load(&p.tm_dres, kSets + b, base + kBufB, n, m0 + 32 * c.q, kBufB);
+  static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int n,
+                                               int m0) {
+    const int slot = k % kNL;
+    const uint32_t base = c.buf + slot * kLoadB;
+    c.load(&p.tm_h, slot, base, n, m0 + 32 * c.q, kBufB);
+    if (p.has_dres) c.load(&p.tm_dres, kNL + slot, base + kBufB, n, m0 + 32 * c.q, kBufB);
   }
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
                                                   int m0, int n0) {
-    c.stores_read_but_last();
-    load_set(p, c, c.cnt % kSets, n0, m0);
+    for (int i = 0; i < kNL - 1; ++i) issue(p, c, c.cnt + i, n0 + i * 32, m0);
   }
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
@@ -536,31 +540,32 @@ struct EpiNormBwd {
     const float k2 = rr * rr * ss;
     const int prow = (m0 >> 5) + c.q;  // partial row (32 rows each)
     for (int ch = 0; ch < NCH; ++ch) {
-      const int b = c.cnt % kSets;
-      const uint32_t hbuf = c.buf + b * kSetB;
+      const int slot = c.cnt % kNL;
+      const uint32_t hbuf = c.buf + slot * kLoadB;
       const uint32_t rbuf = hbuf + kBufB;
+      const uint32_t obuf = c.buf + kNL * kLoadB + (c.cnt & 1) * kBufB;
       c.stores_read_but_last();
-      if (ch + 1 < NCH) load_set(p, c, (c.cnt + 1) % kSets, n0 + (ch + 1) * 32, m0);
+      if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, n0 + (ch + kNL - 1) * 32, m0);
       float P[32], h[32], gm[32];
       tmem_ld32(taddr + ch * 32, P);
       load_nvec32(p.gamma, n0 + ch * 32, g.N, gm);
-      if (!c.wait(b, 13)) return false;
+      if (!c.wait(slot, 13)) return false;
       read_bf16x32(hbuf, c.lane, h);
       float dh[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) dh[j] = gm[j] * P[j] - k2 * h[j];
       if (p.has_dres) {
-        if (!c.wait(kSets + b, 14)) return false;
+        if (!c.wait(kNL + slot, 14)) return false;
         float rz[32];
         read_bf16x32(rbuf, c.lane, rz);
 #pragma unroll
         for (int j = 0; j < 32; ++j) dh[j] += rz[j];
       }
-      stage_bf16x32(hbuf, c.lane, dh);
+      stage_bf16x32(obuf, c.lane, dh);
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
-        tma_store_2d(&p.tm_dh, hbuf, n0 + ch * 32, m0 + 32 * c.q);
+        tma_store_2d(&p.tm_dh, obuf, n0 + ch * 32, m0 + 32 * c.q);
         bulk_commit();
       }
 #pragma unroll
