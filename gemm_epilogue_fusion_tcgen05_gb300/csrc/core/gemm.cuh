@@ -33,7 +33,8 @@ constexpr int kEpiBars = 8;     // mbarriers per epilogue warp (tile loads)
 struct GemmArgs {
   int M, N, K;
   int tiles_m, tiles_n, num_tiles, num_kb;
-  int n_fast;                     // 1: the n-block index varies fastest in tile order
+  int group;                      // tiles are ordered in bands of `group` row (or column) blocks
+  int along_m;                    // 1: bands of row blocks (row index fastest inside a band)
   int* err;                       // device error word
   unsigned long long timeout_ns;  // bound on every wait
 };
@@ -108,13 +109,26 @@ struct GemmTraits {
   static constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN, A_MN, B_MN);
 };
 
+// Grouped tile order. With along_m, the tiles form bands of `group` row
+// blocks; inside a band the row block varies fastest, then the column block.
+// The concurrently running tiles then share a few operand panels: the
+// band's A panels stay in L2 while B panels stream past, each read from HBM
+// once per band. (along_m = 0 is the same with rows and columns swapped.)
 __device__ __forceinline__ void tile_coords(const GemmArgs& g, int t, int& mb, int& nb) {
-  if (g.n_fast) {
-    nb = t % g.tiles_n;
-    mb = t / g.tiles_n;
+  if (g.along_m) {
+    const int per = g.group * g.tiles_n;
+    const int band = t / per, r = t - band * per;
+    const int m0 = band * g.group;
+    const int gs = min(g.group, g.tiles_m - m0);
+    mb = m0 + r % gs;
+    nb = r / gs;
   } else {
-    mb = t % g.tiles_m;
-    nb = t / g.tiles_m;
+    const int per = g.group * g.tiles_m;
+    const int band = t / per, r = t - band * per;
+    const int n0 = band * g.group;
+    const int gs = min(g.group, g.tiles_n - n0);
+    nb = n0 + r % gs;
+    mb = r / gs;
   }
 }
 

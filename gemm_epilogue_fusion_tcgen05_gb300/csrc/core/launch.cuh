@@ -9,6 +9,36 @@
 
 namespace coda {
 
+// Tile order for an M x N x K GEMM with bm x bn tiles: keep the stationary
+// operand's panels of one band within an L2 budget and stream the other.
+// If all of A (or B) fits the budget it stays resident and the other operand
+// streams exactly once; otherwise bands are sized to the budget and the
+// direction with the smaller re-read volume is chosen.
+inline void choose_tile_order(GemmArgs& g, int bm, int bn, int K) {
+  const double budget = 48.0 * 1024 * 1024;
+  const double pa = 2.0 * bm * K, pb = 2.0 * bn * K;  // bytes of one row / column panel
+  const double a_tot = pa * g.tiles_m, b_tot = pb * g.tiles_n;
+  if (a_tot <= budget) {
+    g.along_m = 1;
+    g.group = g.tiles_m;
+  } else if (b_tot <= budget) {
+    g.along_m = 0;
+    g.group = g.tiles_n;
+  } else {
+    const int gm = budget / pa >= 1.0 ? (int)(budget / pa) : 1;
+    const int gn = budget / pb >= 1.0 ? (int)(budget / pb) : 1;
+    const double cost_m = a_tot + b_tot * ((g.tiles_m + gm - 1) / gm);
+    const double cost_n = b_tot + a_tot * ((g.tiles_n + gn - 1) / gn);
+    if (cost_m <= cost_n) {
+      g.along_m = 1;
+      g.group = gm < g.tiles_m ? gm : g.tiles_m;
+    } else {
+      g.along_m = 0;
+      g.group = gn < g.tiles_n ? gn : g.tiles_n;
+    }
+  }
+}
+
 template <class T>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB,
                         const typename T::Epi::Params& ep, int M, int N, int K, const LaunchCtx& lc) {
@@ -31,9 +61,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB,
   g.tiles_n = (N + T::BN - 1) / T::BN;
   g.num_tiles = g.tiles_m * g.tiles_n;
   g.num_kb = (K + kBK - 1) / kBK;
-  // B much larger than A (e.g. an LM head): walk all row blocks of one column
-  // block before the next, so each B panel is read from HBM once.
-  g.n_fast = M > N ? 1 : 0;
+  choose_tile_order(g, kBM, T::BN, K);
   g.err = lc.err;
   g.timeout_ns = lc.timeout_ns;
   const int grid = g.num_tiles < lc.num_sms ? g.num_tiles : lc.num_sms;
@@ -82,7 +110,7 @@ cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
   g.tiles_n = (N + T::BN - 1) / T::BN;
   g.num_tiles = g.tiles_m * g.tiles_n;
   g.num_kb = (K + kBK - 1) / kBK;
-  g.n_fast = M > N ? 1 : 0;
+  choose_tile_order(g, 2 * kBM, T::BN, K);
   g.err = lc.err;
   g.timeout_ns = lc.timeout_ns;
   const int pairs = g.num_tiles < pairs_max ? g.num_tiles : pairs_max;
