@@ -426,12 +426,11 @@ struct EpiCE {
 //   spart[nb, m] = sum (dg g + du u) ; dyhat = r (dg, du) (bf16)
 // Per 16-column chunk of da: one fp32 box of y (32 columns) in, one bf16 box
 // of dyhat (32 columns) out. A ring of kNL load slots keeps the y boxes of
-// the next kNL-1 chunks in flight (this epilogue reads 4 bytes of y per
-// MMA column, so its loads must run far ahead); two store sets.
+// the next kNL-1 chunks in flight; two store sets.
 struct EpiSwiGLUBwd {
   static constexpr int kYBufB = 4096;   // 32 rows x 32 fp32
   static constexpr int kOBufB = 2048;   // 32 rows x 32 bf16
-  static constexpr int kNL = 5;
+  static constexpr int kNL = 3;
   static constexpr int kSmemPerWarp = kNL * kYBufB + 2 * kOBufB;
   struct Params {
     CUtensorMap tm_y, tm_dy;
@@ -507,7 +506,7 @@ struct EpiSwiGLUBwd {
 // store sets of dh.
 struct EpiNormBwd {
   static constexpr int kBufB = 2048;
-  static constexpr int kNL = 4;
+  static constexpr int kNL = 3;
   static constexpr int kLoadB = 2 * kBufB;
   static constexpr int kSmemPerWarp = kNL * kLoadB + 2 * kBufB;
   struct Params {

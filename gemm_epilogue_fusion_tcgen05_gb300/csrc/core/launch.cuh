@@ -3,38 +3,47 @@
 // once while the smaller one stays resident in L2.
 #pragma once
 #include <atomic>
+#include <cmath>
 #include "../internal.h"
 #include "epilogues.cuh"
 #include "gemm2.cuh"
 
 namespace coda {
 
-// Tile order for an M x N x K GEMM with bm x bn tiles: keep the stationary
-// operand's panels of one band within an L2 budget and stream the other.
-// If all of A (or B) fits the budget it stays resident and the other operand
-// streams exactly once; otherwise bands are sized to the budget and the
-// direction with the smaller re-read volume is chosen.
-inline void choose_tile_order(GemmArgs& g, int bm, int bn, int K) {
+// Tile order for an M x N x K GEMM with bm x bn tiles and `conc` tiles in
+// flight at a time. Tiles go in bands of `group` row blocks (or column
+// blocks); the estimate of HBM traffic for a band size G is:
+//   * if the band's stationary panels (G of them) fit an L2 budget, they
+//     are read once and the moving operand's panels stream once per band;
+//   * otherwise nothing survives from one wave of `conc` tiles to the next,
+//     and each wave reads the distinct panels it touches.
+// The direction and G with the smallest estimate win. Small operands that
+// fit the budget whole simply stay resident (G = all blocks).
+inline void choose_tile_order(GemmArgs& g, int bm, int bn, int K, int conc) {
   const double budget = 48.0 * 1024 * 1024;
   const double pa = 2.0 * bm * K, pb = 2.0 * bn * K;  // bytes of one row / column panel
-  const double a_tot = pa * g.tiles_m, b_tot = pb * g.tiles_n;
-  if (a_tot <= budget) {
-    g.along_m = 1;
-    g.group = g.tiles_m;
-  } else if (b_tot <= budget) {
-    g.along_m = 0;
-    g.group = g.tiles_n;
-  } else {
-    const int gm = budget / pa >= 1.0 ? (int)(budget / pa) : 1;
-    const int gn = budget / pb >= 1.0 ? (int)(budget / pb) : 1;
-    const double cost_m = a_tot + b_tot * ((g.tiles_m + gm - 1) / gm);
-    const double cost_n = b_tot + a_tot * ((g.tiles_n + gn - 1) / gn);
-    if (cost_m <= cost_n) {
-      g.along_m = 1;
-      g.group = gm < g.tiles_m ? gm : g.tiles_m;
-    } else {
-      g.along_m = 0;
-      g.group = gn < g.tiles_n ? gn : g.tiles_n;
+  double best = -1.0;
+  for (int dir = 0; dir < 2; ++dir) {
+    const int ts = dir == 0 ? g.tiles_m : g.tiles_n;  // blocks of the stationary operand
+    const int to = dir == 0 ? g.tiles_n : g.tiles_m;  // blocks of the moving operand
+    const double ps = dir == 0 ? pa : pb, po = dir == 0 ? pb : pa;
+    for (int G = 1; G <= ts; ++G) {
+      const int bands = (ts + G - 1) / G;
+      double band_cost;
+      if (G * ps <= budget) {
+        band_cost = G * ps + to * po;
+      } else {
+        const double waves = std::ceil((double)G * to / conc);
+        const double gs = G < conc ? G : conc;
+        const double os = std::ceil((double)conc / G) < to ? std::ceil((double)conc / G) : to;
+        band_cost = waves * (gs * ps + os * po);
+      }
+      const double cost = bands * band_cost;
+      if (best < 0 || cost < best * 0.999) {
+        best = cost;
+        g.along_m = dir == 0 ? 1 : 0;
+        g.group = G;
+      }
     }
   }
 }
@@ -61,7 +70,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB,
   g.tiles_n = (N + T::BN - 1) / T::BN;
   g.num_tiles = g.tiles_m * g.tiles_n;
   g.num_kb = (K + kBK - 1) / kBK;
-  choose_tile_order(g, kBM, T::BN, K);
+  choose_tile_order(g, kBM, T::BN, K, g.num_tiles < lc.num_sms ? g.num_tiles : lc.num_sms);
   g.err = lc.err;
   g.timeout_ns = lc.timeout_ns;
   const int grid = g.num_tiles < lc.num_sms ? g.num_tiles : lc.num_sms;
@@ -110,10 +119,10 @@ cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
   g.tiles_n = (N + T::BN - 1) / T::BN;
   g.num_tiles = g.tiles_m * g.tiles_n;
   g.num_kb = (K + kBK - 1) / kBK;
-  choose_tile_order(g, 2 * kBM, T::BN, K);
+  const int pairs = g.num_tiles < pairs_max ? g.num_tiles : pairs_max;
+  choose_tile_order(g, 2 * kBM, T::BN, K, pairs);
   g.err = lc.err;
   g.timeout_ns = lc.timeout_ns;
-  const int pairs = g.num_tiles < pairs_max ? g.num_tiles : pairs_max;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   e = cudaLaunchKernelEx(&cfg, gemm2_kernel<T>, tmA, tmB, ep, g);
   if (e != cudaSuccess) return e;
