@@ -119,6 +119,25 @@ def _kernel_hash():
     return h.hexdigest()[:16]
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(ms: float, device) -> float:
+    """Largest per-step time over all ranks (every rank holds a replica of
+    the whole step; the slowest one sets the job's step time)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, world: int, ms: float) -> float:
+    """Whole-job TFLOP/s: every replica does a full step in `ms` (the max
+    over ranks)."""
+    return flops_per_step * world / (ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ the step
 
 class Step:
@@ -337,11 +356,8 @@ def run_coda(args):
         for k in range(n):
             per_call[k] += evs[i][k][0].elapsed_time(evs[i][k][1])
     per_call = [t / args.steps for t in per_call]
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = step.flops * ws / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(ms, dev)
+    value = job_throughput(step.flops, ws, ms)
 
     # end-to-end through the public API with host buffers: copy this step's
     # inputs host -> device from pinned memory, run, read the results back
@@ -366,7 +382,7 @@ def run_coda(args):
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
     e2e_ms /= max(e2e_steps, 1)
-    e2e_value = step.flops * ws / (e2e_ms * 1e-3) / 1e12 if e2e_ms > 0 else None
+    e2e_value = job_throughput(step.flops, ws, max_over_ranks(e2e_ms, dev)) if e2e_ms > 0 else None
 
     peaks, src = _peaks()
     k_dom = max(range(n), key=lambda k: per_call[k])
