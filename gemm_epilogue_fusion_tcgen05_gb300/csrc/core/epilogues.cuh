@@ -144,7 +144,7 @@ struct EpiPlain {
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
-        tma_store_2d(&p.tm_c, buf, n0 + ch * 32, m0 + 32 * c.q);
+        c.store(&p.tm_c, buf, n0 + ch * 32, m0 + 32 * c.q);
         bulk_commit();
       }
       ++c.cnt;
@@ -211,8 +211,8 @@ struct EpiResidNormStats {
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
-        tma_store_2d(&p.tm_h, hbuf, n0 + ch * 32, m0 + 32 * c.q);
-        tma_store_2d(&p.tm_hg, gbuf, n0 + ch * 32, m0 + 32 * c.q);
+        c.store(&p.tm_h, hbuf, n0 + ch * 32, m0 + 32 * c.q);
+        c.store(&p.tm_hg, gbuf, n0 + ch * 32, m0 + 32 * c.q);
         bulk_commit();
       }
       ++c.cnt;
@@ -277,8 +277,8 @@ struct EpiRowScaleSwiGLU {
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
-        tma_store_2d(&p.tm_a, abuf, (n0 + ch * 32) / 2, m0 + 32 * c.q);
-        if (p.save_y) tma_store_2d(&p.tm_y, ybuf, n0 + ch * 32, m0 + 32 * c.q);
+        c.store(&p.tm_a, abuf, (n0 + ch * 32) / 2, m0 + 32 * c.q);
+        if (p.save_y) c.store(&p.tm_y, ybuf, n0 + ch * 32, m0 + 32 * c.q);
         bulk_commit();
       }
       ++c.cnt;
@@ -349,8 +349,8 @@ struct EpiRope {
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
-        tma_store_2d(&p.tm_out, buf, col0, m0 + 32 * c.q);
-        if (p.save) tma_store_2d(&p.tm_save, sbuf, col0, m0 + 32 * c.q);
+        c.store(&p.tm_out, buf, col0, m0 + 32 * c.q);
+        if (p.save) c.store(&p.tm_save, sbuf, col0, m0 + 32 * c.q);
         bulk_commit();
       }
       ++c.cnt;
@@ -487,7 +487,7 @@ struct EpiSwiGLUBwd {
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
-        tma_store_2d(&p.tm_dy, obuf, 2 * (n0 + ch * 16), m0 + 32 * c.q);
+        c.store(&p.tm_dy, obuf, 2 * (n0 + ch * 16), m0 + 32 * c.q);
         bulk_commit();
       }
       ++c.cnt;
@@ -564,7 +564,7 @@ struct EpiNormBwd {
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
-        tma_store_2d(&p.tm_dh, obuf, n0 + ch * 32, m0 + 32 * c.q);
+        c.store(&p.tm_dh, obuf, n0 + ch * 32, m0 + 32 * c.q);
         bulk_commit();
       }
 #pragma unroll

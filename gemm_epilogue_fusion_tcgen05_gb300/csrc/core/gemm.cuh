@@ -48,6 +48,7 @@ struct EpiCtx {
   uint32_t pending;  // barriers with a load issued and not yet waited on
   uint32_t cnt;      // chunks processed so far (selects the staging set)
   int lane, q;       // lane; TMEM lane quarter = row block of 32 inside the tile
+  uint64_t pol;      // L2 policy for data touched once (epilogue tile loads and stores)
   DevError e;
 
   __device__ __forceinline__ uint32_t bar(int j) const { return bar0 + 8u * j; }
@@ -56,7 +57,7 @@ struct EpiCtx {
                                        uint32_t bytes) {
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(j), bytes);
-      tma_load_2d(m, dst, bar(j), x, y);
+      tma_load_2d_hint(m, dst, bar(j), x, y, pol);
     }
     pending |= 1u << j;
   }
@@ -72,6 +73,10 @@ struct EpiCtx {
     for (int j = 0; j < kEpiBars; ++j)
       if (pending & (1u << j)) mbar_drain(bar(j), (phase >> j) & 1u, 50000000ull);
     pending = 0;
+  }
+  // store one staged box (lane 0 issues)
+  __device__ __forceinline__ void store(const CUtensorMap* m, uint32_t src, int x, int y) {
+    tma_store_2d_hint(m, src, x, y, pol);
   }
   // lane 0 makes sure every earlier TMA store has finished reading its smem
   __device__ __forceinline__ void stores_read_done() {
@@ -288,6 +293,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     ctx.cnt = 0;
     ctx.lane = lane;
     ctx.q = warp & 3;
+    ctx.pol = l2_policy_evict_first();
     ctx.e = e;
     int li = 0;
     for (int t = blockIdx.x; t < g.num_tiles; t += gridDim.x, ++li) {

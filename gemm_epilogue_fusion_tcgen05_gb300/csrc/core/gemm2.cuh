@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_par = 0;
       bool ok = true;
+      const uint64_t pol_keep = l2_policy_evict_last();
       for (int t = pair; t < g.num_tiles && ok; t += npairs) {
         int mb, nb;
         tile_coords(g, t, mb, nb);
@@ -125,17 +126,27 @@ __global__ void __launch_bounds__(T::kThreads, 1)
           const uint32_t a_dst = sA + stage * T::A_BYTES;
           const uint32_t b_dst = sB + stage * T::B_BYTES;
           const int k0 = kb * kBK;
+          // the band's stationary operand stays in L2 (evict_last); the
+          // other streams past with the default policy
           if constexpr (!T::A_MN) {
-            tma_load_2d_pair(&tmA, a_dst, fb, k0, m0);
+            if (g.along_m) tma_load_2d_pair_hint(&tmA, a_dst, fb, k0, m0, pol_keep);
+            else tma_load_2d_pair(&tmA, a_dst, fb, k0, m0);
           } else {
 #pragma unroll
-            for (int j = 0; j < kBM / 64; ++j) tma_load_2d_pair(&tmA, a_dst + j * 8192, fb, m0 + j * 64, k0);
+            for (int j = 0; j < kBM / 64; ++j) {
+              if (g.along_m) tma_load_2d_pair_hint(&tmA, a_dst + j * 8192, fb, m0 + j * 64, k0, pol_keep);
+              else tma_load_2d_pair(&tmA, a_dst + j * 8192, fb, m0 + j * 64, k0);
+            }
           }
           if constexpr (!T::B_MN) {
-            tma_load_2d_pair(&tmB, b_dst, fb, k0, n0);
+            if (!g.along_m) tma_load_2d_pair_hint(&tmB, b_dst, fb, k0, n0, pol_keep);
+            else tma_load_2d_pair(&tmB, b_dst, fb, k0, n0);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 128; ++j) tma_load_2d_pair(&tmB, b_dst + j * 8192, fb, n0 + j * 64, k0);
+            for (int j = 0; j < BN / 128; ++j) {
+              if (!g.along_m) tma_load_2d_pair_hint(&tmB, b_dst + j * 8192, fb, n0 + j * 64, k0, pol_keep);
+              else tma_load_2d_pair(&tmB, b_dst + j * 8192, fb, n0 + j * 64, k0);
+            }
           }
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -209,6 +220,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     ctx.cnt = 0;
     ctx.lane = lane;
     ctx.q = warp & 3;
+    ctx.pol = l2_policy_evict_first();
     ctx.e = e;
     int li = 0;
     for (int t = pair; t < g.num_tiles; t += npairs, ++li) {
