@@ -431,12 +431,78 @@ def run_coda(args):
     }
     if args.only:
         line["config"]["only"] = args.only
+    if not args.only and not args.no_unfused:
+        ref_ms = unfused_reference(step, flush)
+        line["unfused_reference"] = {
+            "what": "PyTorch eager bf16 on the same inputs: cuBLAS matmuls, separate residual, "
+                    "rms_norm, SiLU*mul, RoPE and cross_entropy kernels (logits materialised), "
+                    "autograd backward",
+            "ms_per_step": round(ref_ms, 4), "value": round(step.flops / (ref_ms * 1e-3) / 1e12, 2),
+            "unit": UNIT, "fused_speedup": round(ref_ms / ms, 3)}
     if rank == 0 and not args.no_cpu_baseline and not args.only:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------ unfused GPU reference
+
+def unfused_reference(step, flush, steps=3, warmup=2):
+    """The same step written the way a framework runs it unfused (PyTorch
+    eager, bf16): cuBLAS GEMMs plus separate elementwise / normalisation /
+    loss kernels, autograd for the backward. Reported as a reference point;
+    it runs none of this library's kernels."""
+    import torch.nn.functional as F
+    s1, i1 = step.s1, step.i1
+    i2 = step.i2
+    d = s1.d
+
+    def leaf(t):
+        return t.detach().clone().requires_grad_(True)
+
+    def one():
+        x, z, W0, W1, W2, gm = (leaf(i1[k]) for k in ("x", "z", "W0", "W1", "W2", "gamma"))
+        h = x @ W0 + z
+        y = F.rms_norm(h, (d,), gm, 1e-6) @ W1
+        out = (F.silu(y[:, 0::2]) * y[:, 1::2]) @ W2
+        out.backward(i1["dout"])
+        logits = i2["hidden"] @ i2["W"]
+        F.cross_entropy(logits.float(), i2["targets"].long(), reduction="none")
+        if step.with_8b:
+            s4, i4 = step.s4, step.i4
+            o, z4, Wo, W14, W24, g2, g1, Wq = (leaf(i4[k]) for k in
+                                               ("o", "z", "Wo", "W1", "W2", "gamma2", "gamma1", "Wqkv"))
+            h4 = o @ Wo + z4
+            y4 = F.rms_norm(h4, (s4.d,), g2, 1e-6) @ W14
+            out4 = (F.silu(y4[:, 0::2]) * y4[:, 1::2]) @ W24 + h4
+            pre = F.rms_norm(out4, (s4.d,), g1, 1e-6) @ Wq
+            nr, hd = s4.n_rope_cols, s4.head_dim
+            pos = torch.arange(s4.M, device=o.device) % s4.seq_len
+            inv = torch.pow(torch.tensor(s4.theta, dtype=torch.float64, device=o.device),
+                            -2.0 * torch.arange(hd // 2, device=o.device, dtype=torch.float64) / hd)
+            ang = (pos[:, None].double() * inv[None, :]).float().repeat(1, nr // hd)
+            c, sn = torch.cos(ang), torch.sin(ang)
+            e, od = pre[:, :nr:2].float(), pre[:, 1:nr:2].float()
+            rot = torch.stack([e * c - od * sn, e * sn + od * c], dim=-1).reshape(s4.M, nr)
+            qkv = torch.cat([rot.to(pre.dtype), pre[:, nr:]], dim=1)
+            torch.autograd.backward([qkv, out4], [i4["dqkv"], i4["dres"]])
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for i in range(steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        one()
+        b.record()
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    torch.cuda.empty_cache()
+    return tot / steps
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -529,6 +595,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-8b", action="store_true", help="leave the 8B-shaped block out of the step")
+    ap.add_argument("--no-unfused", action="store_true",
+                    help="skip the unfused PyTorch reference sequence")
     ap.add_argument("--only", default="", help="time only these calls (comma-separated names; "
                     "profiling aid, not a bench line)")
     args = ap.parse_args()
