@@ -312,6 +312,55 @@ def lse_two_level(logits, tile: int) -> np.ndarray:
     return Mx + np.log(np.sum(ss * np.exp(ms - Mx[:, None]), axis=1))
 
 
+def lmhead_ce_bwd(hidden, W, targets, dloss) -> Dict[str, np.ndarray]:
+    """Backward of the per-token loss for L = sum_i dloss_i * loss_i [notes s2
+    "Cross-entropy loss"; thread Pattern 3, which computes it "as in Cut
+    Cross Entropy"]: with p = softmax(hidden W) per row and e_t the one-hot
+    target row,
+        G       = dloss[:, None] * (p - e_t)
+        dhidden = G W^T ,  dW = hidden^T G
+    """
+    hidden = np.asarray(hidden, dtype=f64)
+    W = np.asarray(W, dtype=f64)
+    t = np.asarray(targets, dtype=np.int64)
+    dloss = np.asarray(dloss, dtype=f64)
+    logits = hidden @ W
+    m = np.max(logits, axis=1)
+    p = np.exp(logits - m[:, None])
+    p /= np.sum(p, axis=1)[:, None]
+    G = p
+    G[np.arange(G.shape[0]), t] -= 1.0
+    G *= dloss[:, None]
+    return {"G": G, "dhidden": G @ W.T, "dW": hidden.T @ G}
+
+
+def lmhead_ce_dW_columns(hidden, W, targets, dloss, cols, chunk: int = 8192) -> np.ndarray:
+    """Columns ``cols`` of dW = hidden^T G for inputs too large to hold all
+    logits: the per-row log-sum-exp over the whole vocabulary is taken chunk
+    by chunk (per-chunk max and sum-exp, combined as in ``lse_two_level``),
+    then G[:, cols] = dloss * (exp(logits[:, cols] - LSE) - onehot)."""
+    hidden = np.asarray(hidden, dtype=f64)
+    W = np.asarray(W, dtype=f64)
+    t = np.asarray(targets, dtype=np.int64)
+    dloss = np.asarray(dloss, dtype=f64)
+    V = W.shape[1]
+    ms, ss = [], []
+    for c0 in range(0, V, chunk):
+        blk = hidden @ W[:, c0:c0 + chunk]
+        mj = np.max(blk, axis=1)
+        ms.append(mj)
+        ss.append(np.sum(np.exp(blk - mj[:, None]), axis=1))
+    ms = np.stack(ms, axis=1)
+    ss = np.stack(ss, axis=1)
+    Mx = np.max(ms, axis=1)
+    lse = Mx + np.log(np.sum(ss * np.exp(ms - Mx[:, None]), axis=1))
+    cols = np.asarray(cols, dtype=np.int64)
+    Gc = np.exp(hidden @ W[:, cols] - lse[:, None])
+    Gc -= (t[:, None] == cols[None, :])
+    Gc *= dloss[:, None]
+    return hidden.T @ Gc
+
+
 # --------------------------------------------------------------------------
 # Llama-3-8B-shaped non-attention block (output projection .. QKV + RoPE)
 # --------------------------------------------------------------------------

@@ -279,6 +279,50 @@ def test_lse_two_level_equals_definition():
     assert rel(O.lse_two_level(logits + c[:, None], 100) - c, direct) < 1e-12
 
 
+def test_ce_backward_finite_differences_and_torch():
+    rng = np.random.default_rng(19)
+    M, d, V = 4, 6, 11
+    hidden = rng.standard_normal((M, d))
+    W = rng.standard_normal((d, V)) * 0.7
+    t = rng.integers(0, V, M)
+    dloss = rng.standard_normal(M)
+    res = O.lmhead_ce_bwd(hidden, W, t, dloss)
+
+    def L(h, w):
+        return float(np.sum(dloss * O.lmhead_ce(h, w, t)["loss"]))
+
+    for name, X in (("dhidden", hidden), ("dW", W)):
+        fd = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            Xp = X.copy(); Xp[idx] += 1e-6
+            Xm = X.copy(); Xm[idx] -= 1e-6
+            args_p = (Xp, W) if name == "dhidden" else (hidden, Xp)
+            args_m = (Xm, W) if name == "dhidden" else (hidden, Xm)
+            fd[idx] = (L(*args_p) - L(*args_m)) / 2e-6
+        assert rel(res[name], fd) < 1e-6, name
+    th = torch.tensor(hidden, requires_grad=True)
+    tw = torch.tensor(W, requires_grad=True)
+    loss = F.cross_entropy(th @ tw, torch.from_numpy(t), reduction="none")
+    (loss * torch.from_numpy(dloss)).sum().backward()
+    assert rel(res["dhidden"], th.grad.numpy()) < 1e-13
+    assert rel(res["dW"], tw.grad.numpy()) < 1e-13
+    # each row of G sums to zero (softmax sums to one, so does the one-hot row)
+    assert np.max(np.abs(res["G"].sum(1))) < 1e-14
+
+
+def test_ce_backward_columns_match_full_form():
+    rng = np.random.default_rng(20)
+    M, d, V = 7, 5, 300
+    hidden = rng.standard_normal((M, d))
+    W = rng.standard_normal((d, V))
+    t = rng.integers(0, V, M)
+    dloss = rng.standard_normal(M)
+    full = O.lmhead_ce_bwd(hidden, W, t, dloss)["dW"]
+    cols = np.array([0, 1, 17, t[0], 299])
+    for chunk in (7, 64, 300, 1000):
+        assert rel(O.lmhead_ce_dW_columns(hidden, W, t, dloss, cols, chunk), full[:, cols]) < 1e-13
+
+
 # ---------------------------------------------------------------- RoPE
 
 def test_rope_frequencies_closed_form():
