@@ -17,7 +17,8 @@ __all__ = [
     "coda_gemm_rowscale_swiglu", "coda_gemm_rope", "coda_rope_table", "coda_lmhead_ce",
     "coda_lmhead_ce_workspace_size", "coda_gemm_rowscale_swiglu_bwd", "coda_row_rms_bwd",
     "coda_gemm_resid_norm_stats_bwd", "coda_col_reduce", "coda_gemm_rope_bwd",
-    "coda_selftest_bounded_wait", "coda_lmhead_ce_noalloc",
+    "coda_selftest_bounded_wait", "coda_lmhead_ce_noalloc", "coda_lmhead_ce_bwd",
+    "coda_lmhead_ce_bwd_workspace_size",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoda.so")
@@ -50,6 +51,8 @@ EXPORTS = {
     "coda_col_reduce": (_I, [_P, _I, _I, _P, _P]),
     "coda_gemm_rope_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _P]),
     "coda_selftest_bounded_wait": (_I, [_I, _P]),
+    "coda_lmhead_ce_bwd_workspace_size": (_Z, [_I, _I]),
+    "coda_lmhead_ce_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _P]),
     "coda_lmhead_ce_noalloc_capacity": (_Z, []),
     "coda_lmhead_ce_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
 }
@@ -145,8 +148,9 @@ def coda_gemm(A, B, C, *, transA=False, transB=False, resid=None, rowsq_part=Non
         raise ValueError("A / C row mismatch")
     if (B.shape[1] if transB else B.shape[0]) != K or (B.shape[0] if transB else B.shape[1]) != N:
         raise ValueError("B shape mismatch")
-    if resid is not None and (resid.shape != C.shape or resid.stride() != C.stride()):
-        raise ValueError("resid must have C's shape and strides")
+    if resid is not None and (resid.shape != C.shape or resid.stride() != C.stride()
+                              or resid.dtype != C.dtype):
+        raise ValueError("resid must have C's shape, strides and dtype")
     _check(lib().coda_gemm(_ptr(A), A.stride(0), int(transA), _ptr(B), B.stride(0), int(transB),
                            _ptr(resid), _ptr(rowsq_part), _ptr(C), C.stride(0),
                            int(C.dtype == f32), M, N, K, _stream(stream)))
@@ -219,6 +223,26 @@ def coda_lmhead_ce(hidden, W, targets, lse, loss, ws, stream=None):
     _check(lib().coda_lmhead_ce(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(lse), _ptr(loss),
                                 _ptr(ws), ws.numel() * ws.element_size(), M, V, d,
                                 _stream(stream)))
+
+
+def coda_lmhead_ce_bwd_workspace_size(M: int, V: int) -> int:
+    return lib().coda_lmhead_ce_bwd_workspace_size(M, V)
+
+
+def coda_lmhead_ce_bwd(hidden, W, targets, lse, dloss, dhidden, dW, ws, stream=None):
+    """dhidden (fp32 [M, d]) and dW (fp32 [d, V]) of sum(dloss * loss)."""
+    M, d = hidden.shape
+    V = W.shape[1]
+    _req(hidden, bf16, "hidden")
+    _req(W, bf16, "W")
+    _req(targets, i32, "targets", 1)
+    _req(lse, f32, "lse", 1)
+    _req(dloss, f32, "dloss", 1)
+    _req(dhidden, f32, "dhidden")
+    _req(dW, f32, "dW")
+    _check(lib().coda_lmhead_ce_bwd(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(lse), _ptr(dloss),
+                                    _ptr(dhidden), _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(),
+                                    M, V, d, _stream(stream)))
 
 
 def coda_lmhead_ce_noalloc(hidden, W, targets, lse, loss, stream=None):

@@ -19,7 +19,8 @@ import torch
 from . import (coda_col_reduce, coda_gemm, coda_gemm_resid_norm_stats,
                coda_gemm_resid_norm_stats_bwd, coda_gemm_rope, coda_gemm_rope_bwd,
                coda_gemm_rowscale_swiglu, coda_gemm_rowscale_swiglu_bwd, coda_lmhead_ce,
-               coda_lmhead_ce_workspace_size, coda_rope_table, coda_row_rms, coda_row_rms_bwd,
+               coda_lmhead_ce_workspace_size, coda_lmhead_ce_bwd, coda_lmhead_ce_bwd_workspace_size,
+               coda_rope_table, coda_row_rms, coda_row_rms_bwd,
                col_tiles, row_tiles32)
 
 bf16, f32 = torch.bfloat16, torch.float32
@@ -96,6 +97,21 @@ def lmhead_ce(hidden, W, targets, ws: Optional[torch.Tensor] = None,
     loss = out["loss"] if out else _e((M,), f32, dev)
     coda_lmhead_ce(hidden, W, targets, lse, loss, ws)
     return {"lse": lse, "loss": loss}
+
+
+def lmhead_ce_bwd(hidden, W, targets, lse, dloss, ws: Optional[torch.Tensor] = None,
+                  out: Optional[Dict[str, torch.Tensor]] = None) -> Dict[str, torch.Tensor]:
+    """dhidden and dW of sum(dloss * loss), the logits recomputed chunk by
+    chunk and never stored."""
+    M, d = hidden.shape
+    V = W.shape[1]
+    dev = hidden.device
+    if ws is None:
+        ws = torch.empty(coda_lmhead_ce_bwd_workspace_size(M, V), dtype=torch.uint8, device=dev)
+    dh = out["dhidden"] if out else _e((M, d), f32, dev)
+    dW = out["dW"] if out else _e((d, V), f32, dev)
+    coda_lmhead_ce_bwd(hidden, W, targets, lse, dloss, dh, dW, ws)
+    return {"dhidden": dh, "dW": dW}
 
 
 def rope_table(seq_len: int, head_dim: int, theta: float, device) -> torch.Tensor:

@@ -217,15 +217,20 @@ coda_status_t coda_gemm(const void* A, int lda, int transA, const void* B, int l
         "coda_gemm: leading dimension too small");
   CHECK(lda % 8 == 0 && ldb % 8 == 0 && ldc % (c_fp32 ? 4 : 8) == 0,
         "coda_gemm: row strides must be multiples of 16 bytes");
-  CHECK(!(resid || rowsq_part) || (!transA && !transB && !c_fp32),
-        "coda_gemm: resid/rowsq_part need transA=0, transB=0, bf16 output");
+  CHECK(!rowsq_part || (!transA && !transB && !c_fp32),
+        "coda_gemm: rowsq_part needs transA=0, transB=0, bf16 output");
+  CHECK(!resid || (!transA && (c_fp32 || !transB)),
+        "coda_gemm: resid needs transA=0 (and transB=0 for a bf16 output)");
   TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
   PlainArgs a{};
   CHECK_MAP(map_a(&a.tmA, A, lda, transA, M, K));
   CHECK_MAP(map_b(&a.tmB, B, ldb, transB, N, K));
   if (c_fp32) CHECK_MAP(map_f32_32(&a.tmC, C, M, N, ldc));
   else CHECK_MAP(map_bf16_32(&a.tmC, C, M, N, ldc));
-  if (resid) CHECK_MAP(map_bf16_32(&a.tmR, resid, M, N, ldc));
+  if (resid) {
+    if (c_fp32) CHECK_MAP(map_f32_32(&a.tmR, resid, M, N, ldc));
+    else CHECK_MAP(map_bf16_32(&a.tmR, resid, M, N, ldc));
+  }
   a.a_mn = transA != 0;
   a.b_mn = transB == 0;
   a.out_f32 = c_fp32 != 0;
@@ -388,6 +393,92 @@ coda_status_t coda_lmhead_ce(const void* hidden, const void* W, const int32_t* t
   return from_cuda(launch_ce_combine(p.part, nparts, p.tlogit, targets, M, V, lse, loss, lc.err,
                                      lc.stream),
                    "coda_lmhead_ce combine launch");
+}
+
+// Vocabulary columns per chunk of the CE backward: the bf16 gradient chunk
+// [M, chunk] is what stays on chip-near (L2) between the three GEMMs.
+static int ce_bwd_chunk(int M, int V, size_t ws_bytes) {
+  const int vr = (V + 255) / 256 * 256;
+  size_t c = ws_bytes / ((size_t)M * 2) / 256 * 256;
+  if (c > 4096) c = 4096;
+  if (c > (size_t)vr) c = vr;
+  return (int)c;
+}
+
+size_t coda_lmhead_ce_bwd_workspace_size(int M, int V) {
+  if (M <= 0 || V <= 0) return 0;
+  const int vr = (V + 255) / 256 * 256;
+  return (size_t)M * (vr < 4096 ? vr : 4096) * 2;
+}
+
+coda_status_t coda_lmhead_ce_bwd(const void* hidden, const void* W, const int32_t* targets,
+                                 const float* lse, const float* dloss, float* dhidden, float* dW,
+                                 void* ws, size_t ws_bytes, int M, int V, int d,
+                                 coda_stream_t stream) {
+  CHECK_PTR(hidden);
+  CHECK_PTR(W);
+  CHECK_PTR(targets);
+  CHECK_PTR(lse);
+  CHECK_PTR(dloss);
+  CHECK_PTR(dhidden);
+  CHECK_PTR(dW);
+  CHECK_PTR(ws);
+  CHECK(M > 0 && V > 0 && d > 0 && M < kMaxDim && V < kMaxDim && d < kMaxDim,
+        "coda_lmhead_ce_bwd: bad sizes");
+  CHECK(V % 8 == 0 && d % 8 == 0, "coda_lmhead_ce_bwd: V and d must be multiples of 8");
+  const int chunk = ce_bwd_chunk(M, V, ws_bytes);
+  CHECK(chunk >= 256, "coda_lmhead_ce_bwd: workspace too small (%zu bytes; at least %zu)",
+        ws_bytes, (size_t)M * 256 * 2);
+  TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
+  const bf16* Wb = static_cast<const bf16*>(W);
+  for (int v0 = 0; v0 < V; v0 += chunk) {
+    const int vc = V - v0 < chunk ? V - v0 : chunk;
+    // (1) logits of this chunk, recomputed; the epilogue forms G in bf16
+    CEGradArgs g{};
+    CHECK_MAP(map_a(&g.tmA, hidden, d, 0, M, d));
+    CHECK_MAP(tmap2d(&g.tmB, Wb + v0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vc, d, V, 64, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+    CHECK_MAP(map_bf16_32(&g.tm_g, ws, M, vc, chunk));
+    g.targets = targets;
+    g.lse = lse;
+    g.dloss = dloss;
+    g.v0 = v0;
+    g.M = M;
+    g.N = vc;
+    g.K = d;
+    coda_status_t s = from_cuda(launch_ce_grad(g, lc), "coda_lmhead_ce_bwd logits launch");
+    if (s != CODA_OK) return s;
+    // (2) dhidden (+)= G W_chunk^T, fp32, accumulated over the chunks
+    PlainArgs h{};
+    CHECK_MAP(map_a(&h.tmA, ws, chunk, 0, M, vc));
+    CHECK_MAP(tmap2d(&h.tmB, Wb + v0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vc, d, V, 64,
+                     kTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B));
+    CHECK_MAP(map_f32_32(&h.tmC, dhidden, M, d, d));
+    if (v0 > 0) CHECK_MAP(map_f32_32(&h.tmR, dhidden, M, d, d));
+    h.a_mn = false;
+    h.b_mn = false;
+    h.out_f32 = true;
+    h.resid = v0 > 0;
+    h.M = M;
+    h.N = d;
+    h.K = vc;
+    s = from_cuda(launch_plain(h, lc), "coda_lmhead_ce_bwd dhidden launch");
+    if (s != CODA_OK) return s;
+    // (3) dW[:, v0 : v0 + vc] = hidden^T G
+    PlainArgs w{};
+    CHECK_MAP(map_a(&w.tmA, hidden, d, 1, d, M));
+    CHECK_MAP(map_b(&w.tmB, ws, chunk, 0, vc, M));
+    CHECK_MAP(map_f32_32(&w.tmC, dW + v0, d, vc, V));
+    w.a_mn = true;
+    w.b_mn = true;
+    w.out_f32 = true;
+    w.M = d;
+    w.N = vc;
+    w.K = M;
+    s = from_cuda(launch_plain(w, lc), "coda_lmhead_ce_bwd dW launch");
+    if (s != CODA_OK) return s;
+  }
+  return CODA_OK;
 }
 
 coda_status_t coda_gemm_rowscale_swiglu_bwd(const void* dout, const void* W2, const void* y,

@@ -79,16 +79,17 @@ __device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
 
 // ------------------------------------------------------------------ plain
 // C = acc (+ resid), optional per-row sum of squares of the stored value's
-// fp32 pre-image. fp32 output rows are 128 bytes per 32 columns, bf16 64.
+// fp32 pre-image. fp32 output rows are 128 bytes per 32 columns, bf16 64;
+// the residual has the output's type (an fp32 residual may be C itself:
+// C += A B).
 // Two store sets; with a residual, a ring of kNL load slots keeps the
 // residual boxes of the next kNL-1 chunks in flight.
 template <bool OUT_F32, bool RESID, bool ROWSQ>
 struct EpiPlain {
-  static_assert(!(OUT_F32 && RESID), "residual is defined for bf16 outputs");
   static constexpr int kRowB = OUT_F32 ? 128 : 64;
   static constexpr int kBufB = 32 * kRowB;
-  static constexpr int kNL = RESID ? 4 : 0;  // load slots (32 rows x 32 bf16 each)
-  static constexpr int kLoadB = 2048;
+  static constexpr int kNL = RESID ? (OUT_F32 ? 3 : 4) : 0;  // load slots, one box each
+  static constexpr int kLoadB = kBufB;  // the residual has the output's type
   static constexpr int kSmemPerWarp = kNL * kLoadB + 2 * kBufB;
   struct Params {
     CUtensorMap tm_c;
@@ -123,10 +124,22 @@ struct EpiPlain {
       if constexpr (RESID) {
         const int slot = c.cnt % kNL;
         if (!c.wait(slot, 10)) return false;
-        float z[32];
-        read_bf16x32(c.buf + slot * kLoadB, c.lane, z);
+        const uint32_t lb = c.buf + slot * kLoadB;
+        if constexpr (OUT_F32) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] += z[j];
+          for (int k = 0; k < 8; ++k) {
+            const uint4 u = ld_shared_v4(lb + swz<128>(c.lane, k));
+            v[4 * k] += __uint_as_float(u.x);
+            v[4 * k + 1] += __uint_as_float(u.y);
+            v[4 * k + 2] += __uint_as_float(u.z);
+            v[4 * k + 3] += __uint_as_float(u.w);
+          }
+        } else {
+          float z[32];
+          read_bf16x32(lb, c.lane, z);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += z[j];
+        }
       }
       if constexpr (ROWSQ) {
 #pragma unroll
@@ -410,6 +423,60 @@ struct EpiCE {
     if (row < g.M) {
       p.part[(size_t)nb * g.M + row] = make_float2(rmax, rsum);
       if (tgt >= n0 && tgt < n0 + BN && tgt < g.N) p.tlogit[row] = tl;
+    }
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------ CE backward
+// LM-head cross-entropy backward, one vocabulary chunk at a time (the
+// logits are recomputed, never stored; "Reading notes on CODA", s2
+// "Cross-entropy loss", thread Pattern 3 "as in Cut Cross Entropy"):
+//   G[m, v] = dloss[m] * (exp(logit[m, v] - lse[m]) - [v == target[m]])
+// stored in bf16 into the chunk buffer; v is the chunk's first column v0
+// plus the tile column.
+struct EpiCEGrad {
+  static constexpr int kBufB = 2048;  // 32 rows x 32 bf16
+  static constexpr int kSmemPerWarp = 2 * kBufB;
+  struct Params {
+    CUtensorMap tm_g;
+    const int* targets;
+    const float* lse;
+    const float* dloss;
+    int v0;
+  };
+  template <int BN>
+  static __device__ __forceinline__ void prefetch(const Params&, EpiCtx&, const GemmArgs&, int, int) {}
+  template <int BN>
+  static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
+                                              int n0, int, uint32_t taddr) {
+    constexpr int NCH = BN / 32;
+    const int row = m0 + 32 * c.q + c.lane;
+    const bool live = row < g.M;
+    const int tgt = live ? __ldg(p.targets + row) : -1;
+    const float l0 = live ? __ldg(p.lse + row) : 0.f;
+    const float dl = live ? __ldg(p.dloss + row) : 0.f;
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int col0 = n0 + ch * 32;
+      if (col0 >= g.N) break;
+      const uint32_t buf = c.buf + (c.cnt & 1) * kBufB;
+      c.stores_read_but_last();
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      const int gcol0 = p.v0 + col0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float pj = __expf(v[j] - l0);
+        v[j] = dl * (gcol0 + j == tgt ? pj - 1.0f : pj);
+      }
+      stage_bf16x32(buf, c.lane, v);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (c.lane == 0) {
+        c.store(&p.tm_g, buf, col0, m0 + 32 * c.q);
+        bulk_commit();
+      }
+      ++c.cnt;
     }
     return true;
   }

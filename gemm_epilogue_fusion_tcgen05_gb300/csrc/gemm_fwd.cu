@@ -53,4 +53,16 @@ cudaError_t launch_ce(const CEArgs& a, const LaunchCtx& lc) {
   return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
+cudaError_t launch_ce_grad(const CEGradArgs& a, const LaunchCtx& lc) {
+  using E = EpiCEGrad;
+  using T = Gemm2Traits<kTileN, false, true, E>;
+  E::Params p;
+  p.tm_g = a.tm_g;
+  p.targets = a.targets;
+  p.lse = a.lse;
+  p.dloss = a.dloss;
+  p.v0 = a.v0;
+  return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+}
+
 }  // namespace coda

@@ -19,7 +19,8 @@ cudaError_t launch_plain_other(const PlainArgs& a, const LaunchCtx& lc);
 
 cudaError_t launch_plain(const PlainArgs& a, const LaunchCtx& lc) {
   if (!a.a_mn && a.b_mn) {
-    if (a.out_f32) return plain_impl<false, true, true, false, false>(a, lc);
+    if (a.out_f32) return a.resid ? plain_impl<false, true, true, true, false>(a, lc)
+                                  : plain_impl<false, true, true, false, false>(a, lc);
     if (a.resid && a.rowsq) return plain_impl<false, true, false, true, true>(a, lc);
     if (a.resid) return plain_impl<false, true, false, true, false>(a, lc);
     if (a.rowsq) return plain_impl<false, true, false, false, true>(a, lc);

@@ -4,9 +4,9 @@
 
 namespace coda {
 
-template <bool AMN, bool BMN, bool F32>
+template <bool AMN, bool BMN, bool F32, bool R = false>
 static cudaError_t plain_t_impl(const PlainArgs& a, const LaunchCtx& lc) {
-  using E = EpiPlain<F32, false, false>;
+  using E = EpiPlain<F32, R, false>;
   using T = Gemm2Traits<kTileN, AMN, BMN, E>;
   typename E::Params p;
   p.tm_c = a.tmC;
@@ -16,7 +16,12 @@ static cudaError_t plain_t_impl(const PlainArgs& a, const LaunchCtx& lc) {
 }
 
 cudaError_t launch_plain_other(const PlainArgs& a, const LaunchCtx& lc) {
-  if (a.resid || a.rowsq) return cudaErrorNotSupported;
+  if (a.rowsq) return cudaErrorNotSupported;
+  if (a.resid) {
+    // C (+)= A B^T in fp32: e.g. a gradient accumulated over several launches
+    if (!a.a_mn && !a.b_mn && a.out_f32) return plain_t_impl<false, false, true, true>(a, lc);
+    return cudaErrorNotSupported;
+  }
   if (!a.a_mn && !a.b_mn)
     return a.out_f32 ? plain_t_impl<false, false, true>(a, lc) : plain_t_impl<false, false, false>(a, lc);
   if (a.a_mn && a.b_mn)

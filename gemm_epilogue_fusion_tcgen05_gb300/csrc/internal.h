@@ -61,6 +61,16 @@ struct CEArgs {
 };
 cudaError_t launch_ce(const CEArgs& a, const LaunchCtx& lc);
 
+struct CEGradArgs {
+  CUtensorMap tmA, tmB, tm_g;
+  const int* targets;
+  const float* lse;
+  const float* dloss;
+  int v0;
+  int M, N, K;
+};
+cudaError_t launch_ce_grad(const CEGradArgs& a, const LaunchCtx& lc);
+
 struct SwiGLUBwdArgs {
   CUtensorMap tmA, tmB, tm_y, tm_dy;
   const float* r;

@@ -90,11 +90,13 @@ const char* coda_last_error_string(void);
  *   C[M, N] = op(A) op(B) (+ resid)
  *   transA = 0: A is [M, K] (lda >= K); 1: A is stored [K, M] (lda >= M).
  *   transB = 0: B is [K, N] (ldb >= N); 1: B is stored [N, K] (ldb >= K).
- *   resid (nullable, bf16 [M, N], row stride ldc) is added in fp32 before
- *   rounding; rowsq_part (nullable, fp32 [coda_col_tiles(N), M]) receives
+ *   resid (nullable, [M, N] of C's type, row stride ldc) is added in fp32
+ *   before rounding; rowsq_part (nullable, fp32 [coda_col_tiles(N), M]) receives
  *   sum over each 256-column tile of the fp32 result squared.
  *   c_fp32 = 1: C is fp32 (e.g. weight gradients), else bf16.
- *   resid / rowsq_part require transA = 0, transB = 0 and c_fp32 = 0. */
+ *   rowsq_part requires transA = 0, transB = 0, c_fp32 = 0. resid requires
+ *   transA = 0; with c_fp32 = 0 it is bf16 and needs transB = 0, with
+ *   c_fp32 = 1 it is fp32 (and may be C itself: C += op(A) op(B)). */
 coda_status_t coda_gemm(const void* A, int lda, int transA, const void* B, int ldb, int transB,
                         const void* resid, float* rowsq_part, void* C, int ldc, int c_fp32,
                         int M, int N, int K, coda_stream_t stream);
@@ -192,6 +194,27 @@ size_t coda_lmhead_ce_noalloc_capacity(void);
 coda_status_t coda_lmhead_ce_noalloc(const void* hidden, const void* W, const int32_t* targets,
                                      float* lse, float* loss, int M, int V, int d,
                                      coda_stream_t stream);
+
+/* Bytes of scratch that coda_lmhead_ce_bwd uses for M rows and V classes
+ * (one bf16 gradient chunk of M x min(V rounded up to 256, 4096)). */
+size_t coda_lmhead_ce_bwd_workspace_size(int M, int V);
+
+/* LM-head cross-entropy backward without materialising the logits
+ * ([notes] s2 "Cross-entropy loss"; [thread] Pattern 3, "as in Cut Cross
+ * Entropy"; the pages give no backward, this is the reading): for
+ * L = sum_m dloss[m] * loss[m],
+ *   G = dloss[m] (softmax(hidden W)[m] - onehot(targets[m]))
+ *   dhidden = G W^T (fp32 [M, d]),  dW = hidden^T G (fp32 [d, V])
+ * The vocabulary is processed in chunks: per chunk, a GEMM recomputes the
+ * logit tile and its epilogue writes G (bf16) into ws; a second GEMM adds
+ * G W_chunk^T into dhidden; a third writes dW's columns of the chunk.
+ * lse: fp32 [M] from coda_lmhead_ce. ws: caller-owned scratch; its size
+ * sets the chunk width (at least M * 256 * 2 bytes; see
+ * coda_lmhead_ce_bwd_workspace_size). Other arguments as in coda_lmhead_ce. */
+coda_status_t coda_lmhead_ce_bwd(const void* hidden, const void* W, const int32_t* targets,
+                                 const float* lse, const float* dloss, float* dhidden, float* dW,
+                                 void* ws, size_t ws_bytes, int M, int V, int d,
+                                 coda_stream_t stream);
 
 /* ------------------------------------------------------------ backward */
 
