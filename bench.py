@@ -431,6 +431,8 @@ def run_coda(args):
     }
     if args.only:
         line["config"]["only"] = args.only
+    if not args.only:
+        line["next_rows"] = next_rows(step, flush)
     if not args.only and not args.no_unfused:
         ref_ms = unfused_reference(step, flush)
         line["unfused_reference"] = {
@@ -445,6 +447,40 @@ def run_coda(args):
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------ rows beyond the step
+
+def next_rows(step, flush, reps=5):
+    """Kernels built beyond the step's rows, timed on the step's LM-head
+    inputs: the cross-entropy backward (logits recomputed per vocabulary
+    chunk; three GEMMs of 2*M*d*V each)."""
+    C = step.C
+    s2, i2 = step.s2, step.i2
+    dev = step.dev
+    dl = torch.full((s2.M,), 1.0 / s2.M, dtype=torch.float32, device=dev)
+    dh = torch.empty((s2.M, s2.d), dtype=torch.float32, device=dev)
+    dW = torch.empty((s2.d, s2.V), dtype=torch.float32, device=dev)
+    ws = torch.empty(C.coda_lmhead_ce_bwd_workspace_size(s2.M, s2.V), dtype=torch.uint8, device=dev)
+    fn = lambda: C.coda_lmhead_ce_bwd(i2["hidden"], i2["W"], i2["targets"], step.o2["lse"], dl,
+                                      dh, dW, ws)
+    fn()
+    torch.cuda.synchronize()
+    ts = []
+    for i in range(reps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = sorted(ts)[len(ts) // 2]
+    fl = 3 * 2.0 * s2.M * s2.d * s2.V
+    chunk = min(4096, (s2.V + 255) // 256 * 256)
+    return {"lmhead_ce_bwd": {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+                              "tokens_per_s": round(s2.M / (ms * 1e-3), 1),
+                              "launches": 3 * ((s2.V + chunk - 1) // chunk)}}
 
 
 # ------------------------------------------------------------------ unfused GPU reference
