@@ -490,7 +490,9 @@ def unfused_reference(step, flush, steps=3, warmup=2):
     eager, bf16): cuBLAS GEMMs plus separate elementwise / normalisation /
     loss kernels, autograd for the backward. Reported as a reference point;
     it runs none of this library's kernels."""
+    import warnings
     import torch.nn.functional as F
+    warnings.filterwarnings("ignore", message="Attempting to run cuBLAS")
     s1, i1 = step.s1, step.i1
     i2 = step.i2
     d = s1.d

@@ -84,6 +84,9 @@ def test_ce_bwd_full_size(coda):
     dWc = O.lmhead_ce_dW_columns(O.to64(inp["hidden"]), Wd, inp["targets"].numpy(),
                                  dl.double().numpy(), cols)
     assert_close("dW (sampled columns)", bw["dW"].cpu()[:, cols], dWc, TOL_BF16)
-    # every row of G sums to zero, so every row of dW sums to zero
-    rs = bw["dW"].double().sum(1).abs().max().item()
-    assert rs < 1e-3 * bw["dW"].abs().max().item()
+    # every row of G sums to zero, so every row of dW sums to zero up to the
+    # bf16 rounding of G: at most a few bf16 units of the row's 2-norm
+    dW64 = bw["dW"].double()
+    ratio = (dW64.sum(1).abs() / dW64.norm(dim=1)).max().item()
+    print(f"max |row sum of dW| / ||row||_2 = {ratio:.3e}")
+    assert ratio < 1e-2
