@@ -543,6 +543,83 @@ def unfused_reference(step, flush, steps=3, warmup=2):
     return tot / steps
 
 
+# ------------------------------------------------------------------ primitive microbenchmarks
+
+def run_primitives(args):
+    """One GEMM shape (8192 x 8192 x 4096, bf16) with one epilogue primitive
+    of each class ("Reading notes on CODA", s1; the pages' Fig. 8 measures
+    the same kind of table on H100), fused here vs cuBLAS followed by a
+    separate PyTorch kernel:
+      elementwise/pairwise map   SwiGLU on adjacent columns
+      row/column vector load     row scale r[m] (delayed RMSNorm factor)
+      tile load/store            residual add
+      tile reduction             per-row sum of squares
+      stateful transform         running max / sum-exp (LSE + CE, V = N)"""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__ as g
+    g.build()
+    import gemm_epilogue_fusion_tcgen05_gb300 as C
+    import torch.nn.functional as F
+    gen = torch.Generator(device=dev).manual_seed(7)
+    M, N, K = 8192, 8192, 4096
+    bf, f32 = torch.bfloat16, torch.float32
+    A = torch.randn(M, K, device=dev, generator=gen).to(bf)
+    B = (torch.randn(K, N, device=dev, generator=gen) * 0.02).to(bf)
+    R = torch.randn(M, N, device=dev, generator=gen).to(bf)
+    r = torch.rand(M, device=dev, generator=gen) + 0.5
+    t = torch.randint(0, N, (M,), device=dev, generator=gen, dtype=torch.int32)
+    out = torch.empty(M, N, dtype=bf, device=dev)
+    half = torch.empty(M, N // 2, dtype=bf, device=dev)
+    part = torch.empty(C.col_tiles(N), M, dtype=f32, device=dev)
+    cs = torch.zeros(16, 64, 2, dtype=f32, device=dev)
+    lse = torch.empty(M, dtype=f32, device=dev)
+    loss = torch.empty(M, dtype=f32, device=dev)
+    ws = torch.empty(C.coda_lmhead_ce_workspace_size(M, N), dtype=torch.uint8, device=dev)
+    flush = torch.empty(128 * 1024 * 1024, dtype=f32, device=dev)
+
+    def timeit(fn, reps=7):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for i in range(reps):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return sorted(ts)[len(ts) // 2]
+
+    cases = {
+        "pairwise map (SwiGLU)": (
+            lambda: C.coda_gemm_rowscale_swiglu(A, B, torch.ones_like(r), half, None),
+            lambda: (lambda y: F.silu(y[:, 0::2]) * y[:, 1::2])(A @ B)),
+        "row vector (scale r[m])": (
+            lambda: C.coda_gemm_rope(A, B, r, cs, 16, 128, 0, out),
+            lambda: (A @ B) * r[:, None].to(bf)),
+        "tile load (residual)": (
+            lambda: C.coda_gemm(A, B, out, resid=R),
+            lambda: A @ B + R),
+        "tile reduction (row sum of squares)": (
+            lambda: C.coda_gemm(A, B, out, rowsq_part=part),
+            lambda: (lambda y: (y, y.float().square().sum(1)))(A @ B)),
+        "stateful max/sum-exp (LSE + CE)": (
+            lambda: C.coda_lmhead_ce(A, B, t, lse, loss, ws),
+            lambda: F.cross_entropy((A @ B).float(), t.long(), reduction="none")),
+    }
+    gemm_ms = timeit(lambda: torch.matmul(A, B, out=out))
+    res = {}
+    for name, (fused, unfused) in cases.items():
+        fm, um = timeit(fused), timeit(unfused)
+        res[name] = {"fused_ms": round(fm, 4), "cublas_plus_kernel_ms": round(um, 4),
+                     "speedup": round(um / fm, 3)}
+    line = {"metric": "epilogue primitives: fused GEMM+epilogue vs cuBLAS + separate kernel",
+            "shape": [M, N, K], "cublas_gemm_alone_ms": round(gemm_ms, 4), "primitives": res}
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 def _oracle_sample(rows1, rows_ce, rows8):
@@ -633,6 +710,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-8b", action="store_true", help="leave the 8B-shaped block out of the step")
+    ap.add_argument("--primitives", action="store_true",
+                    help="epilogue-primitive microbenchmarks instead of the step")
     ap.add_argument("--no-unfused", action="store_true",
                     help="skip the unfused PyTorch reference sequence")
     ap.add_argument("--only", default="", help="time only these calls (comma-separated names; "
@@ -641,7 +720,9 @@ def main():
     if args.warmup < 3:
         print("note: at least 3 warm-up steps are required; using 3", file=sys.stderr)
         args.warmup = 3
-    if args.impl == "reference":
+    if args.primitives:
+        run_primitives(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_coda(args)
