@@ -237,6 +237,114 @@ def mlp_bwd_reparam(fwd: Dict[str, np.ndarray], x, W0, W1, W2, gamma, dout,
 
 
 # --------------------------------------------------------------------------
+# LayerNorm variant of the block (the pages promise it, they do not work it)
+# --------------------------------------------------------------------------
+
+def ln_mlp_fwd(x, z, W0, W1, W2, gamma, beta, eps: float = EPS) -> Dict[str, np.ndarray]:
+    """Canonical forward with LayerNorm in place of RMSNorm:
+        h = x W0 + z ; mu = mean(h) ; r = 1/sqrt(mean((h - mu)^2) + eps)
+        nh = (h - mu) r ; h2 = nh * gamma + beta ; y = h2 W1
+        a = silu(y_gate) * y_up ; out = a W2
+    """
+    x, z, W0, W1, W2, gamma, beta = (np.asarray(t, dtype=f64) for t in (x, z, W0, W1, W2, gamma, beta))
+    h = x @ W0 + z
+    mu = np.mean(h, axis=1)
+    hc = h - mu[:, None]
+    r = 1.0 / np.sqrt(np.mean(hc * hc, axis=1) + eps)
+    nh = hc * r[:, None]
+    h2 = nh * gamma[None, :] + beta[None, :]
+    y = h2 @ W1
+    a = swiglu(y)
+    out = a @ W2
+    return {"h": h, "mu": mu, "r": r, "nh": nh, "h2": h2, "y": y, "a": a, "out": out}
+
+
+def ln_mlp_bwd(fwd, x, W0, W1, W2, gamma, beta, dout) -> Dict[str, np.ndarray]:
+    """Canonical backward of ``ln_mlp_fwd`` for L = sum(dout * out); the
+    LayerNorm backward is dh = r (dnh - mean(dnh) - nh mean(dnh * nh)),
+    dnh = gamma * dh2."""
+    x, W0, W1, W2, gamma, beta, dout = (np.asarray(t, dtype=f64) for t in
+                                        (x, W0, W1, W2, gamma, beta, dout))
+    h, r, nh, h2, y, a = (fwd[k] for k in ("h", "r", "nh", "h2", "y", "a"))
+    da = dout @ W2.T
+    dW2 = a.T @ dout
+    g = y[:, 0::2]
+    u = y[:, 1::2]
+    dy = np.empty_like(y)
+    dy[:, 0::2] = da * u * silu_grad(g)
+    dy[:, 1::2] = da * silu(g)
+    dW1 = h2.T @ dy
+    dh2 = dy @ W1.T
+    dgamma = np.sum(dh2 * nh, axis=0)
+    dbeta = np.sum(dh2, axis=0)
+    dnh = gamma[None, :] * dh2
+    sa = np.mean(dnh, axis=1)
+    sb = np.mean(dnh * nh, axis=1)
+    dh = r[:, None] * (dnh - sa[:, None] - nh * sb[:, None])
+    return {"dy": dy, "sa": sa, "sb": sb, "dh": dh, "dz": dh, "dx": dh @ W0.T,
+            "dW0": x.T @ dh, "dW1": dW1, "dW2": dW2, "dgamma": dgamma, "dbeta": dbeta}
+
+
+def ln_mlp_fwd_reparam(x, z, W0, W1, W2, gamma, beta, eps: float = EPS,
+                       store_bf16: bool = False) -> Dict[str, np.ndarray]:
+    """Rewritten LayerNorm forward (this library's reading, following the
+    pages' RMSNorm rewrite [notes s2]): GEMM 1's epilogue stores h and
+    hg = h * gamma and emits per-row sums of h and h^2; the auxiliary step
+    gives mu and r; with the n-vectors w1 = gamma W1 and b1 = beta W1,
+        y = r (hg W1) - (r mu) w1 + b1
+    which equals (r (h - mu) gamma + beta) W1."""
+    st = _store(store_bf16)
+    x, z, W0, W1, W2, gamma, beta = (np.asarray(t, dtype=f64) for t in (x, z, W0, W1, W2, gamma, beta))
+    h_acc = x @ W0 + z
+    d = h_acc.shape[1]
+    s1 = np.sum(h_acc, axis=1)
+    s2 = np.sum(h_acc * h_acc, axis=1)
+    mu = s1 / d
+    r = 1.0 / np.sqrt(np.maximum(s2 / d - mu * mu, 0.0) + eps)
+    h = st(h_acc)
+    hg = st(h_acc * gamma[None, :])
+    w1 = gamma @ W1
+    b1 = beta @ W1
+    y = r[:, None] * (hg @ W1) - (r * mu)[:, None] * w1[None, :] + b1[None, :]
+    a = st(swiglu(y))
+    out = st(a @ W2)
+    return {"h": h, "hg": hg, "mu": mu, "r": r, "w1": w1, "b1": b1, "y": y, "a": a, "out": out}
+
+
+def ln_mlp_bwd_reparam(fwd, x, W0, W1, W2, gamma, beta, dout,
+                       store_bf16: bool = False) -> Dict[str, np.ndarray]:
+    """Rewritten LayerNorm backward: both statistics move into the epilogue
+    of the GEMM that produces dy (as s does in [notes s3]):
+        s_a = (1/d) sum_k dy_k w1_k ,  s_b = (1/d) (sum_k dy_k y_k - sum_k dy_k b1_k)
+    and with dyhat = r dy, P = dyhat W1^T (= r dh2):
+        dh = gamma P - r s_a - r^2 (h - mu) s_b
+        dgamma = sum_rows P (h - mu) ,  dbeta = sum_rows P / r
+        dW1 = hhat^T dyhat with hhat = (h - mu) gamma + beta / r (= h2 / r)
+    """
+    st = _store(store_bf16)
+    x, W0, W1, W2, gamma, beta, dout = (np.asarray(t, dtype=f64) for t in
+                                        (x, W0, W1, W2, gamma, beta, dout))
+    h, hg, mu, r, w1, b1, y, a = (fwd[k] for k in ("h", "hg", "mu", "r", "w1", "b1", "y", "a"))
+    d = h.shape[1]
+    da = dout @ W2.T
+    g = y[:, 0::2]
+    u = y[:, 1::2]
+    dy = np.empty_like(y)
+    dy[:, 0::2] = da * u * silu_grad(g)
+    dy[:, 1::2] = da * silu(g)
+    sa = (dy @ w1) / d
+    sb = (np.sum(dy * y, axis=1) - dy @ b1) / d
+    dyhat = st(r[:, None] * dy)
+    P = dyhat @ W1.T
+    hc = h - mu[:, None]
+    dh = st(gamma[None, :] * P - (r * sa)[:, None] - (r * r * sb)[:, None] * hc)
+    hhat = st(hc * gamma[None, :] + beta[None, :] / r[:, None])
+    return {"dy": dy, "sa": sa, "sb": sb, "dyhat": dyhat, "P": P, "dh": dh, "dz": dh,
+            "hhat": hhat, "dgamma": np.sum(P * hc, axis=0), "dbeta": np.sum(P / r[:, None], axis=0),
+            "dW1": hhat.T @ dyhat, "dW2": a.T @ dout, "dx": st(dh @ W0.T), "dW0": x.T @ dh}
+
+
+# --------------------------------------------------------------------------
 # RoPE on adjacent pairs
 # --------------------------------------------------------------------------
 

@@ -224,6 +224,80 @@ def test_storage_rounded_mode_rounds_stored_tensors_only():
     assert rel(fr["out"], fe["out"]) < 2e-2
 
 
+def rand_ln_block(M=3, d=8, f=8, seed=30):
+    inp = rand_block(M, d, f, seed)
+    inp["beta"] = np.random.default_rng(seed + 1).standard_normal(d) * 0.3
+    return inp
+
+
+def test_ln_block_matches_torch_layer_norm_and_autograd():
+    inp = rand_ln_block(M=5, d=16, f=12, seed=31)
+    t = {k: torch.tensor(v, dtype=torch.float64, requires_grad=k != "dout") for k, v in inp.items()}
+    h = t["x"] @ t["W0"] + t["z"]
+    h2 = F.layer_norm(h, (16,), t["gamma"], t["beta"], 1e-6)
+    y = h2 @ t["W1"]
+    out = (F.silu(y[:, 0::2]) * y[:, 1::2]) @ t["W2"]
+    (out * t["dout"]).sum().backward()
+    args = [inp[k] for k in ("x", "z", "W0", "W1", "W2", "gamma", "beta")]
+    fw = O.ln_mlp_fwd(*args)
+    bw = O.ln_mlp_bwd(fw, inp["x"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"], inp["beta"],
+                      inp["dout"])
+    assert rel(fw["out"], out.detach().numpy()) < 1e-13
+    for k, g in (("x", "dx"), ("z", "dz"), ("W0", "dW0"), ("W1", "dW1"), ("W2", "dW2"),
+                 ("gamma", "dgamma"), ("beta", "dbeta")):
+        assert rel(bw[g], t[k].grad.numpy()) < 1e-12, k
+
+
+def test_ln_block_finite_differences():
+    inp = rand_ln_block(M=2, d=6, f=4, seed=32)
+    keys = ("x", "z", "W0", "W1", "W2", "gamma", "beta")
+
+    def L(v):
+        return float(np.sum(O.ln_mlp_fwd(*[v[k] for k in keys])["out"] * inp["dout"]))
+
+    fw = O.ln_mlp_fwd(*[inp[k] for k in keys])
+    bw = O.ln_mlp_bwd(fw, inp["x"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"], inp["beta"],
+                      inp["dout"])
+    for k, gname in zip(keys, ("dx", "dz", "dW0", "dW1", "dW2", "dgamma", "dbeta")):
+        fd = np.zeros_like(inp[k])
+        for idx in np.ndindex(inp[k].shape):
+            v = {kk: np.array(inp[kk], copy=True) for kk in keys}
+            v[k][idx] += 1e-6
+            lp = L(v)
+            v[k][idx] -= 2e-6
+            fd[idx] = (lp - L(v)) / 2e-6
+        assert rel(bw[gname], fd) < 1e-6, k
+
+
+def test_ln_reparam_equals_canonical():
+    inp = rand_ln_block(M=7, d=24, f=16, seed=33)
+    args = [inp[k] for k in ("x", "z", "W0", "W1", "W2", "gamma", "beta")]
+    fc = O.ln_mlp_fwd(*args)
+    fr = O.ln_mlp_fwd_reparam(*args)
+    for k in ("mu", "r", "y", "a", "out"):
+        assert rel(fr[k], fc[k]) < 1e-12, k
+    bargs = (inp["x"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"], inp["beta"], inp["dout"])
+    bc = O.ln_mlp_bwd(fc, *bargs)
+    br = O.ln_mlp_bwd_reparam(fr, *bargs)
+    for k in ("sa", "sb", "dh", "dx", "dW0", "dW1", "dW2", "dgamma", "dbeta"):
+        assert rel(br[k], bc[k]) < 1e-11, k
+    assert rel(br["hhat"] * fr["r"][:, None], fc["h2"]) < 1e-12
+    frs = O.ln_mlp_fwd_reparam(*args, store_bf16=True)
+    for k in ("h", "hg", "a", "out"):
+        assert np.array_equal(frs[k], O.bf16_round(frs[k])), k
+
+
+def test_ln_with_zero_mean_rows_reduces_to_rmsnorm():
+    # rows whose h has zero mean and beta = 0: LayerNorm equals RMSNorm
+    inp = rand_block(M=4, d=8, f=6, seed=34)
+    inp["W0"] = np.eye(8)
+    inp["z"] = np.zeros((4, 8))
+    inp["x"] = inp["x"] - inp["x"].mean(1, keepdims=True)
+    ln = O.ln_mlp_fwd(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"], np.zeros(8))
+    rm = O.mlp_fwd(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"])
+    assert rel(ln["out"], rm["out"]) < 1e-13
+
+
 # ---------------------------------------------------------------- cross-entropy
 
 def test_ce_zero_weights_closed_form():
