@@ -122,6 +122,25 @@ def mlp_block_inputs(shape: BlockShape, with_grad: bool = True, device="cpu") ->
     return out
 
 
+def ln_block_inputs(shape: BlockShape, with_grad: bool = True, device="cpu") -> Dict[str, torch.Tensor]:
+    """mlp_block_inputs plus the LayerNorm shift beta [d] bf16 ~N(0, 0.3^2),
+    drawn afterwards from the same generator."""
+    g = _gen(shape.seed, device)
+    M, d, f = shape.M, shape.d, shape.f
+    out = {
+        "x": _normal(g, (M, d)),
+        "z": _normal(g, (M, d)),
+        "W0": _normal(g, (d, d), 0.02),
+        "W1": _normal(g, (d, 2 * f), 0.02),
+        "W2": _normal(g, (f, d), 0.02),
+        "gamma": _uniform(g, (d,), 0.5, 1.5),
+    }
+    if with_grad:
+        out["dout"] = _normal(g, (M, d))
+    out["beta"] = _normal(g, (d,), 0.3)
+    return out
+
+
 def lmhead_inputs(shape: LMHeadShape, device="cpu") -> Dict[str, torch.Tensor]:
     """hidden [M,d] bf16 ~N(0,1); W [d,V] bf16 ~N(0,0.02^2); targets int32 [M]."""
     g = _gen(shape.seed, device)

@@ -18,7 +18,9 @@ __all__ = [
     "coda_lmhead_ce_workspace_size", "coda_gemm_rowscale_swiglu_bwd", "coda_row_rms_bwd",
     "coda_gemm_resid_norm_stats_bwd", "coda_col_reduce", "coda_gemm_rope_bwd",
     "coda_selftest_bounded_wait", "coda_lmhead_ce_noalloc", "coda_lmhead_ce_bwd",
-    "coda_lmhead_ce_bwd_workspace_size",
+    "coda_lmhead_ce_bwd_workspace_size", "coda_gemm_resid_ln_stats", "coda_row_ln",
+    "coda_gemm_ln_rowscale_swiglu", "coda_gemm_ln_rowscale_swiglu_bwd", "coda_row_ln_bwd",
+    "coda_gemm_resid_ln_stats_bwd",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoda.so")
@@ -53,6 +55,13 @@ EXPORTS = {
     "coda_selftest_bounded_wait": (_I, [_I, _P]),
     "coda_lmhead_ce_bwd_workspace_size": (_Z, [_I, _I]),
     "coda_lmhead_ce_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _P]),
+    "coda_gemm_resid_ln_stats": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "coda_row_ln": (_I, [_P, _P, _I, _I, _I, _F, _P, _P, _P]),
+    "coda_gemm_ln_rowscale_swiglu": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "coda_gemm_ln_rowscale_swiglu_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I,
+                                              _P]),
+    "coda_row_ln_bwd": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "coda_gemm_resid_ln_stats_bwd": (_I, [_P] * 14 + [_I, _I, _I, _P]),
     "coda_lmhead_ce_noalloc_capacity": (_Z, []),
     "coda_lmhead_ce_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
 }
@@ -243,6 +252,68 @@ def coda_lmhead_ce_bwd(hidden, W, targets, lse, dloss, dhidden, dW, ws, stream=N
     _check(lib().coda_lmhead_ce_bwd(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(lse), _ptr(dloss),
                                     _ptr(dhidden), _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(),
                                     M, V, d, _stream(stream)))
+
+
+# ---------------------------------------------------------------- LayerNorm variant
+
+def coda_gemm_resid_ln_stats(x, W0, z, gamma, h, hg, part_sq, part_sum, stream=None):
+    M, K = x.shape
+    N = W0.shape[1]
+    for t, n in ((x, "x"), (W0, "W0"), (z, "z"), (h, "h"), (hg, "hg")):
+        _req(t, bf16, n)
+    _req(part_sq, f32, "part_sq")
+    _req(part_sum, f32, "part_sum")
+    _check(lib().coda_gemm_resid_ln_stats(_ptr(x), _ptr(W0), _ptr(z), _ptr(gamma), _ptr(h),
+                                          _ptr(hg), _ptr(part_sq), _ptr(part_sum), M, N, K,
+                                          _stream(stream)))
+
+
+def coda_row_ln(part_sq, part_sum, r, mu, d: int, eps: float = 1e-6, stream=None):
+    nparts, M = part_sq.shape
+    _check(lib().coda_row_ln(_ptr(part_sq), _ptr(part_sum), nparts, M, d, eps, _ptr(r), _ptr(mu),
+                             _stream(stream)))
+
+
+def coda_gemm_ln_rowscale_swiglu(hg, W1, r, mu, w1, b1, a, y_save=None, stream=None):
+    M, K = hg.shape
+    two_f = W1.shape[1]
+    _req(hg, bf16, "hg")
+    _req(W1, bf16, "W1")
+    _req(a, bf16, "a")
+    for t, n in ((r, "r"), (mu, "mu"), (w1, "w1"), (b1, "b1")):
+        _req(t, f32, n, 1)
+    if y_save is not None:
+        _req(y_save, f32, "y_save")
+    _check(lib().coda_gemm_ln_rowscale_swiglu(_ptr(hg), _ptr(W1), _ptr(r), _ptr(mu), _ptr(w1),
+                                              _ptr(b1), _ptr(a), _ptr(y_save), M, two_f, K,
+                                              _stream(stream)))
+
+
+def coda_gemm_ln_rowscale_swiglu_bwd(dout, W2, y, r, w1, b1, dyhat, spart, spart_w, spart_b,
+                                     stream=None):
+    M, d = dout.shape
+    f = W2.shape[0]
+    _req(y, f32, "y")
+    _check(lib().coda_gemm_ln_rowscale_swiglu_bwd(_ptr(dout), _ptr(W2), _ptr(y), _ptr(r),
+                                                  _ptr(w1), _ptr(b1), _ptr(dyhat), _ptr(spart),
+                                                  _ptr(spart_w), _ptr(spart_b), M, f, d,
+                                                  _stream(stream)))
+
+
+def coda_row_ln_bwd(spart, spart_w, spart_b, s_a, s_b, d: int, stream=None):
+    nparts, M = spart.shape
+    _check(lib().coda_row_ln_bwd(_ptr(spart), _ptr(spart_w), _ptr(spart_b), nparts, M, d,
+                                 _ptr(s_a), _ptr(s_b), _stream(stream)))
+
+
+def coda_gemm_resid_ln_stats_bwd(dyhat, W1, h, gamma, beta, r, mu, s_a, s_b, dh, dgamma_part,
+                                 dbeta_part, hhat=None, dresid=None, stream=None):
+    M, two_f = dyhat.shape
+    d = W1.shape[0]
+    _check(lib().coda_gemm_resid_ln_stats_bwd(_ptr(dyhat), _ptr(W1), _ptr(h), _ptr(gamma),
+                                              _ptr(beta), _ptr(r), _ptr(mu), _ptr(s_a), _ptr(s_b),
+                                              _ptr(dresid), _ptr(dh), _ptr(hhat), _ptr(dgamma_part),
+                                              _ptr(dbeta_part), M, d, two_f, _stream(stream)))
 
 
 def coda_lmhead_ce_noalloc(hidden, W, targets, lse, loss, stream=None):

@@ -85,6 +85,64 @@ def mlp_block_bwd(fwd: Dict[str, torch.Tensor], x, W0, W1, W2, gamma, dout,
             "dW1": dW1, "dW2": dW2, "dx": dx}
 
 
+def ln_mlp_block_fwd(x, z, W0, W1, W2, gamma, beta, eps: float = 1e-6) -> Dict[str, torch.Tensor]:
+    """LayerNorm variant of mlp_block_fwd: GEMM 1 (+ residual, gamma side
+    output, sum and sum-of-squares partials) -> mu, r -> GEMM 2 (delayed
+    normalisation r (hg W1) - (r mu) w1 + b1, SwiGLU) -> GEMM 3. The
+    n-vectors w1 = gamma W1 and b1 = beta W1 come from two one-row GEMMs
+    (they change only when the weights do)."""
+    from . import (coda_gemm_ln_rowscale_swiglu, coda_gemm_resid_ln_stats, coda_row_ln)
+    M, d = x.shape
+    two_f = W1.shape[1]
+    dev = x.device
+    h, hg = _e((M, d), bf16, dev), _e((M, d), bf16, dev)
+    psq, psum = _e((col_tiles(d), M), f32, dev), _e((col_tiles(d), M), f32, dev)
+    r, mu = _e((M,), f32, dev), _e((M,), f32, dev)
+    w1, b1 = _e((1, two_f), f32, dev), _e((1, two_f), f32, dev)
+    a, y = _e((M, two_f // 2), bf16, dev), _e((M, two_f), f32, dev)
+    out = _e((M, d), bf16, dev)
+    coda_gemm(gamma.view(1, d), W1, w1)
+    coda_gemm(beta.view(1, d), W1, b1)
+    coda_gemm_resid_ln_stats(x, W0, z, gamma, h, hg, psq, psum)
+    coda_row_ln(psq, psum, r, mu, d, eps)
+    coda_gemm_ln_rowscale_swiglu(hg, W1, r, mu, w1.view(-1), b1.view(-1), a, y)
+    coda_gemm(a, W2, out)
+    return {"h": h, "hg": hg, "r": r, "mu": mu, "w1": w1.view(-1), "b1": b1.view(-1), "a": a,
+            "y": y, "out": out}
+
+
+def ln_mlp_block_bwd(fwd: Dict[str, torch.Tensor], x, W0, W1, W2, gamma, beta,
+                     dout) -> Dict[str, torch.Tensor]:
+    """Reverse-fused backward of ln_mlp_block_fwd."""
+    from . import (coda_gemm_ln_rowscale_swiglu_bwd, coda_gemm_resid_ln_stats_bwd,
+                   coda_row_ln_bwd)
+    M, d = x.shape
+    two_f = W1.shape[1]
+    f = two_f // 2
+    dev = x.device
+    dyhat = _e((M, two_f), bf16, dev)
+    sp, spw, spb = (_e((col_tiles(f), M), f32, dev) for _ in range(3))
+    sa, sb = _e((M,), f32, dev), _e((M,), f32, dev)
+    dh, hhat = _e((M, d), bf16, dev), _e((M, d), bf16, dev)
+    dgp, dbp = _e((row_tiles32(M), d), f32, dev), _e((row_tiles32(M), d), f32, dev)
+    dgamma, dbeta = _e((d,), f32, dev), _e((d,), f32, dev)
+    dW0, dW1, dW2 = _e((d, d), f32, dev), _e((d, two_f), f32, dev), _e((f, d), f32, dev)
+    dx = _e((M, d), bf16, dev)
+    coda_gemm_ln_rowscale_swiglu_bwd(dout, W2, fwd["y"], fwd["r"], fwd["w1"], fwd["b1"], dyhat,
+                                     sp, spw, spb)
+    coda_row_ln_bwd(sp, spw, spb, sa, sb, d)
+    coda_gemm_resid_ln_stats_bwd(dyhat, W1, fwd["h"], gamma, beta, fwd["r"], fwd["mu"], sa, sb,
+                                 dh, dgp, dbp, hhat=hhat)
+    coda_col_reduce(dgp, dgamma)
+    coda_col_reduce(dbp, dbeta)
+    coda_gemm(fwd["a"], dout, dW2, transA=True)
+    coda_gemm(hhat, dyhat, dW1, transA=True)
+    coda_gemm(x, dh, dW0, transA=True)
+    coda_gemm(dh, W0, dx, transB=True)
+    return {"dyhat": dyhat, "sa": sa, "sb": sb, "dh": dh, "dz": dh, "hhat": hhat,
+            "dgamma": dgamma, "dbeta": dbeta, "dW0": dW0, "dW1": dW1, "dW2": dW2, "dx": dx}
+
+
 def lmhead_ce(hidden, W, targets, ws: Optional[torch.Tensor] = None,
               out: Optional[Dict[str, torch.Tensor]] = None) -> Dict[str, torch.Tensor]:
     """Per-token LSE and CE loss; the logits never reach memory."""

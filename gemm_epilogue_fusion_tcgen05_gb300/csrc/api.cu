@@ -584,6 +584,192 @@ coda_status_t coda_gemm_rope_bwd(const void* dqkv_rot, const float* qkv_rot, con
                    "coda_gemm_rope_bwd launch");
 }
 
+// ------------------------------------------------------------------ LayerNorm variant
+
+coda_status_t coda_gemm_resid_ln_stats(const void* x, const void* W0, const void* z,
+                                       const void* gamma, void* h, void* hg, float* part_sq,
+                                       float* part_sum, int M, int N, int K, coda_stream_t stream) {
+  CHECK_PTR(x);
+  CHECK_PTR(W0);
+  CHECK_PTR(z);
+  CHECK_PTR(gamma);
+  CHECK_PTR(h);
+  CHECK_PTR(hg);
+  CHECK_PTR(part_sq);
+  CHECK_PTR(part_sum);
+  CHECK(M > 0 && N > 0 && K > 0 && M < kMaxDim && N < kMaxDim && K < kMaxDim,
+        "coda_gemm_resid_ln_stats: bad sizes");
+  CHECK(N % 8 == 0 && K % 8 == 0, "coda_gemm_resid_ln_stats: N and K must be multiples of 8");
+  TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
+  ResidNormStatsArgs a{};
+  CHECK_MAP(map_a(&a.tmA, x, K, 0, M, K));
+  CHECK_MAP(map_b(&a.tmB, W0, N, 0, N, K));
+  CHECK_MAP(map_bf16_32(&a.tm_z, z, M, N, N));
+  CHECK_MAP(map_bf16_32(&a.tm_h, h, M, N, N));
+  CHECK_MAP(map_bf16_32(&a.tm_hg, hg, M, N, N));
+  a.gamma = static_cast<const bf16*>(gamma);
+  a.part = part_sq;
+  a.part2 = part_sum;
+  a.ln = 1;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  return from_cuda(launch_resid_norm_stats(a, lc), "coda_gemm_resid_ln_stats launch");
+}
+
+coda_status_t coda_row_ln(const float* part_sq, const float* part_sum, int nparts, int M, int d,
+                          float eps, float* r, float* mu, coda_stream_t stream) {
+  CHECK_PTR(part_sq);
+  CHECK_PTR(part_sum);
+  CHECK_PTR(r);
+  CHECK_PTR(mu);
+  CHECK(nparts > 0 && M > 0 && d > 0, "coda_row_ln: bad sizes");
+  CHECK(eps >= 0.f, "coda_row_ln: eps must be >= 0");
+  TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
+  return from_cuda(launch_ln_stats(part_sq, part_sum, nparts, M, 1.0f / (float)d, eps, r, mu,
+                                   lc.stream),
+                   "coda_row_ln launch");
+}
+
+coda_status_t coda_gemm_ln_rowscale_swiglu(const void* hg, const void* W1, const float* r,
+                                           const float* mu, const float* w1, const float* b1,
+                                           void* a, float* y_save, int M, int two_f, int K,
+                                           coda_stream_t stream) {
+  CHECK_PTR(hg);
+  CHECK_PTR(W1);
+  CHECK_PTR(r);
+  CHECK_PTR(mu);
+  CHECK_PTR(w1);
+  CHECK_PTR(b1);
+  CHECK_PTR(a);
+  CHECK_OPT_PTR(y_save);
+  CHECK(M > 0 && two_f > 0 && K > 0 && M < kMaxDim && two_f < kMaxDim && K < kMaxDim,
+        "coda_gemm_ln_rowscale_swiglu: bad sizes");
+  CHECK(two_f % 16 == 0 && K % 8 == 0,
+        "coda_gemm_ln_rowscale_swiglu: two_f must be a multiple of 16, K of 8");
+  TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
+  RowScaleSwiGLUArgs p{};
+  CHECK_MAP(map_a(&p.tmA, hg, K, 0, M, K));
+  CHECK_MAP(map_b(&p.tmB, W1, two_f, 0, two_f, K));
+  CHECK_MAP(map_bf16_16(&p.tm_a, a, M, two_f / 2, two_f / 2));
+  if (y_save) CHECK_MAP(map_f32_32(&p.tm_y, y_save, M, two_f, two_f));
+  else p.tm_y = p.tm_a;  // unused
+  p.r = r;
+  p.mu = mu;
+  p.w1 = w1;
+  p.b1 = b1;
+  p.ln = 1;
+  p.save_y = y_save != nullptr;
+  p.M = M;
+  p.N = two_f;
+  p.K = K;
+  return from_cuda(launch_rowscale_swiglu(p, lc), "coda_gemm_ln_rowscale_swiglu launch");
+}
+
+coda_status_t coda_gemm_ln_rowscale_swiglu_bwd(const void* dout, const void* W2, const float* y,
+                                               const float* r, const float* w1, const float* b1,
+                                               void* dyhat, float* spart, float* spart_w,
+                                               float* spart_b, int M, int f, int d,
+                                               coda_stream_t stream) {
+  CHECK_PTR(dout);
+  CHECK_PTR(W2);
+  CHECK_PTR(y);
+  CHECK_PTR(r);
+  CHECK_PTR(w1);
+  CHECK_PTR(b1);
+  CHECK_PTR(dyhat);
+  CHECK_PTR(spart);
+  CHECK_PTR(spart_w);
+  CHECK_PTR(spart_b);
+  CHECK(M > 0 && f > 0 && d > 0 && M < kMaxDim && f < kMaxDim / 2 && d < kMaxDim,
+        "coda_gemm_ln_rowscale_swiglu_bwd: bad sizes");
+  CHECK(f % 8 == 0 && d % 8 == 0,
+        "coda_gemm_ln_rowscale_swiglu_bwd: f and d must be multiples of 8");
+  TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
+  SwiGLUBwdArgs p{};
+  CHECK_MAP(map_a(&p.tmA, dout, d, 0, M, d));
+  CHECK_MAP(map_b(&p.tmB, W2, d, 1, f, d));
+  CHECK_MAP(map_f32_32(&p.tm_y, y, M, 2 * f, 2 * f));
+  CHECK_MAP(map_bf16_32(&p.tm_dy, dyhat, M, 2 * f, 2 * f));
+  p.r = r;
+  p.spart = spart;
+  p.ln = 1;
+  p.w1 = w1;
+  p.b1 = b1;
+  p.spart_w = spart_w;
+  p.spart_b = spart_b;
+  p.M = M;
+  p.N = f;
+  p.K = d;
+  return from_cuda(launch_swiglu_bwd(p, lc), "coda_gemm_ln_rowscale_swiglu_bwd launch");
+}
+
+coda_status_t coda_row_ln_bwd(const float* spart, const float* spart_w, const float* spart_b,
+                              int nparts, int M, int d, float* s_a, float* s_b,
+                              coda_stream_t stream) {
+  CHECK_PTR(spart);
+  CHECK_PTR(spart_w);
+  CHECK_PTR(spart_b);
+  CHECK_PTR(s_a);
+  CHECK_PTR(s_b);
+  CHECK(nparts > 0 && M > 0 && d > 0, "coda_row_ln_bwd: bad sizes");
+  TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
+  return from_cuda(launch_ln_bwd_stats(spart, spart_w, spart_b, nparts, M, 1.0f / (float)d, s_a,
+                                       s_b, lc.stream),
+                   "coda_row_ln_bwd launch");
+}
+
+coda_status_t coda_gemm_resid_ln_stats_bwd(const void* dyhat, const void* W1, const void* h,
+                                           const void* gamma, const void* beta, const float* r,
+                                           const float* mu, const float* s_a, const float* s_b,
+                                           const void* dresid, void* dh, void* hhat,
+                                           float* dgamma_part, float* dbeta_part, int M, int d,
+                                           int two_f, coda_stream_t stream) {
+  CHECK_PTR(dyhat);
+  CHECK_PTR(W1);
+  CHECK_PTR(h);
+  CHECK_PTR(gamma);
+  CHECK_PTR(beta);
+  CHECK_PTR(r);
+  CHECK_PTR(mu);
+  CHECK_PTR(s_a);
+  CHECK_PTR(s_b);
+  CHECK_OPT_PTR(dresid);
+  CHECK_PTR(dh);
+  CHECK_OPT_PTR(hhat);
+  CHECK_PTR(dgamma_part);
+  CHECK_PTR(dbeta_part);
+  CHECK(M > 0 && d > 0 && two_f > 0 && M < kMaxDim && d < kMaxDim && two_f < kMaxDim,
+        "coda_gemm_resid_ln_stats_bwd: bad sizes");
+  CHECK(d % 8 == 0 && two_f % 8 == 0,
+        "coda_gemm_resid_ln_stats_bwd: d and two_f must be multiples of 8");
+  TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
+  NormBwdArgs p{};
+  CHECK_MAP(map_a(&p.tmA, dyhat, two_f, 0, M, two_f));
+  CHECK_MAP(map_b(&p.tmB, W1, two_f, 1, d, two_f));
+  CHECK_MAP(map_bf16_32(&p.tm_h, h, M, d, d));
+  CHECK_MAP(map_bf16_32(&p.tm_dh, dh, M, d, d));
+  if (dresid) CHECK_MAP(map_bf16_32(&p.tm_dres, dresid, M, d, d));
+  else p.tm_dres = p.tm_h;  // unused
+  if (hhat) CHECK_MAP(map_bf16_32(&p.tm_hhat, hhat, M, d, d));
+  else p.tm_hhat = p.tm_h;  // unused
+  p.gamma = static_cast<const bf16*>(gamma);
+  p.beta = static_cast<const bf16*>(beta);
+  p.r = r;
+  p.s = s_b;
+  p.sa = s_a;
+  p.mu = mu;
+  p.dgpart = dgamma_part;
+  p.dbpart = dbeta_part;
+  p.has_dres = dresid != nullptr;
+  p.save_hhat = hhat != nullptr;
+  p.ln = 1;
+  p.M = M;
+  p.N = d;
+  p.K = two_f;
+  return from_cuda(launch_norm_bwd(p, lc), "coda_gemm_resid_ln_stats_bwd launch");
+}
+
 coda_status_t coda_selftest_bounded_wait(int timeout_ms, coda_stream_t stream) {
   CHECK(timeout_ms > 0 && timeout_ms <= 10000, "coda_selftest_bounded_wait: timeout 1..10000 ms");
   TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);

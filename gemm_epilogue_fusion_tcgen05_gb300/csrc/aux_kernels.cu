@@ -175,6 +175,41 @@ __global__ void rope_bwd_kernel(const __nv_bfloat16* __restrict__ d, const float
   }
 }
 
+// LayerNorm statistics from per-tile sums of h^2 and of h:
+//   mu = sum h / d ; r = 1 / sqrt(max(sum h^2 / d - mu^2, 0) + eps)
+__global__ void ln_stats_kernel(const float* __restrict__ psq, const float* __restrict__ psum,
+                                int nparts, int M, float inv_d, float eps, float* __restrict__ r,
+                                float* __restrict__ mu) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  float a = 0.f, b = 0.f;
+  for (int j = 0; j < nparts; ++j) {
+    a += __ldg(psq + (size_t)j * M + m);
+    b += __ldg(psum + (size_t)j * M + m);
+  }
+  const float mean = b * inv_d;
+  const float var = fmaxf(fmaf(a, inv_d, -mean * mean), 0.f);
+  mu[m] = mean;
+  r[m] = 1.0f / sqrtf(var + eps);
+}
+
+// The two relocated LayerNorm-backward statistics:
+//   s_a = sum dy w1 / d ; s_b = (sum dy y - sum dy b1) / d
+__global__ void ln_bwd_stats_kernel(const float* __restrict__ sp, const float* __restrict__ spw,
+                                    const float* __restrict__ spb, int nparts, int M, float inv_d,
+                                    float* __restrict__ sa, float* __restrict__ sb) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  float y = 0.f, w = 0.f, b = 0.f;
+  for (int j = 0; j < nparts; ++j) {
+    y += __ldg(sp + (size_t)j * M + m);
+    w += __ldg(spw + (size_t)j * M + m);
+    b += __ldg(spb + (size_t)j * M + m);
+  }
+  sa[m] = w * inv_d;
+  sb[m] = (y - b) * inv_d;
+}
+
 // A kernel whose only job is to wait on an mbarrier that nothing arrives at,
 // with a short bound: it must give up, record CODA_ERR_TIMEOUT and return.
 // Used by the tests of the bounded-wait machinery.
@@ -223,6 +258,17 @@ cudaError_t launch_rope_bwd(const __nv_bfloat16* d, const float* q, const float*
                             const float2* cs, int seq_len, int head_dim, int n_rope,
                             __nv_bfloat16* out, float* s, int M, int N, float inv_d, cudaStream_t st) {
   rope_bwd_kernel<<<M, 128, 0, st>>>(d, q, r, cs, seq_len, head_dim, n_rope, out, s, M, N, inv_d);
+  return cudaGetLastError();
+}
+cudaError_t launch_ln_stats(const float* part_sq, const float* part_sum, int nparts, int M, float inv_d,
+                            float eps, float* r, float* mu, cudaStream_t st) {
+  ln_stats_kernel<<<(M + 255) / 256, 256, 0, st>>>(part_sq, part_sum, nparts, M, inv_d, eps, r, mu);
+  return cudaGetLastError();
+}
+cudaError_t launch_ln_bwd_stats(const float* spart, const float* spart_w, const float* spart_b,
+                                int nparts, int M, float inv_d, float* sa, float* sb, cudaStream_t st) {
+  ln_bwd_stats_kernel<<<(M + 255) / 256, 256, 0, st>>>(spart, spart_w, spart_b, nparts, M, inv_d,
+                                                       sa, sb);
   return cudaGetLastError();
 }
 cudaError_t launch_bounded_wait_probe(int* err, unsigned long long timeout_ns, cudaStream_t st) {

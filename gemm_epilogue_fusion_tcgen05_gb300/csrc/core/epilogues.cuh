@@ -39,6 +39,22 @@ __device__ __forceinline__ void load_nvec32(const __nv_bfloat16* p, int n, int N
   }
 }
 
+// 32 fp32 values of an n-vector starting at column n (broadcast load).
+// Columns >= N read as 0.
+__device__ __forceinline__ void load_nvec32f(const float* p, int n, int N, float (&o)[32]) {
+  if (n + 32 <= N) {
+    const float4* q = reinterpret_cast<const float4*>(p + n);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float4 u = __ldg(q + k);
+      o[4 * k] = u.x; o[4 * k + 1] = u.y; o[4 * k + 2] = u.z; o[4 * k + 3] = u.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = (n + j < N) ? __ldg(p + n + j) : 0.f;
+  }
+}
+
 // Unpack one 16-byte chunk (8 bf16) from shared memory into o[0..7].
 __device__ __forceinline__ void unpack8(uint4 u, float* o) {
   o[0] = bf16_lo(u.x); o[1] = bf16_hi(u.x); o[2] = bf16_lo(u.y); o[3] = bf16_hi(u.y);
@@ -175,8 +191,10 @@ struct EpiPlain {
 // "Kernel Example": residual D = acc + C, block sum of squares of the
 // unscaled D, side output D * gamma[n]):
 //   h = acc + z (stored), hg = h * gamma (stored), part[nb, m] = sum_n h^2
+// With LN (the LayerNorm variant) also part2[nb, m] = sum_n h.
 // A ring of kNL load slots keeps the z boxes of the next kNL-1 chunks in
 // flight; two store sets of {h, hg}.
+template <bool LN>
 struct EpiResidNormStats {
   static constexpr int kBufB = 2048;  // 32 rows x 32 bf16
   static constexpr int kNL = 4;
@@ -185,7 +203,8 @@ struct EpiResidNormStats {
   struct Params {
     CUtensorMap tm_z, tm_h, tm_hg;
     const __nv_bfloat16* gamma;
-    float* part;  // [tiles_n, M]
+    float* part;   // [tiles_n, M] sums of h^2
+    float* part2;  // [tiles_n, M] sums of h (LN only)
   };
   static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int n,
                                                int m0) {
@@ -201,7 +220,7 @@ struct EpiResidNormStats {
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
                                               int n0, int nb, uint32_t taddr) {
     constexpr int NCH = BN / 32;
-    float ss = 0.f;
+    float ss = 0.f, s1 = 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
       const int slot = c.cnt % kNL;
       const uint32_t hbuf = c.buf + kNL * kBufB + (c.cnt & 1) * kStoreB;
@@ -217,6 +236,7 @@ struct EpiResidNormStats {
       for (int j = 0; j < 32; ++j) {
         v[j] += z[j];
         ss = fmaf(v[j], v[j], ss);
+        if constexpr (LN) s1 += v[j];
         gm[j] *= v[j];
       }
       stage_bf16x32(hbuf, c.lane, v);
@@ -231,7 +251,10 @@ struct EpiResidNormStats {
       ++c.cnt;
     }
     const int row = m0 + 32 * c.q + c.lane;
-    if (row < g.M) p.part[(size_t)nb * g.M + row] = ss;
+    if (row < g.M) {
+      p.part[(size_t)nb * g.M + row] = ss;
+      if constexpr (LN) p.part2[(size_t)nb * g.M + row] = s1;
+    }
     return true;
   }
 };
@@ -243,6 +266,9 @@ struct EpiResidNormStats {
 //   y = r[m] * acc ; a_k = silu(y_2k) * y_2k+1 (bf16) ; y optionally saved in
 //   fp32 for the backward (its relocated RMSNorm statistic sums 2f products
 //   with heavy cancellation, which bf16 storage of y would dominate)
+// With LN (LayerNorm variant): y = r[m] acc - (r mu)[m] w1[n] + b1[n], with
+// the n-vectors w1 = gamma W1 and b1 = beta W1.
+template <bool LN>
 struct EpiRowScaleSwiGLU {
   static constexpr int kABufB = 1024;  // 32 rows x 16 bf16 (32-byte rows)
   static constexpr int kYBufB = 4096;  // 32 rows x 32 fp32 (128-byte rows)
@@ -251,6 +277,9 @@ struct EpiRowScaleSwiGLU {
   struct Params {
     CUtensorMap tm_a, tm_y;
     const float* r;
+    const float* mu;   // LN only
+    const float* w1;   // LN only, [N]
+    const float* b1;   // LN only, [N]
     int save_y;
   };
   template <int BN>
@@ -261,6 +290,8 @@ struct EpiRowScaleSwiGLU {
     constexpr int NCH = BN / 32;
     const int row = m0 + 32 * c.q + c.lane;
     const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
+    float rm = 0.f;
+    if constexpr (LN) rm = row < g.M ? rr * __ldg(p.mu + row) : 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
       const int b = c.cnt & 1;
       const uint32_t abuf = c.buf + b * kSetB;
@@ -268,15 +299,24 @@ struct EpiRowScaleSwiGLU {
       c.stores_read_but_last();
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
+      if constexpr (LN) {
+        float w[32], bb[32];
+        load_nvec32f(p.w1, n0 + ch * 32, g.N, w);
+        load_nvec32f(p.b1, n0 + ch * 32, g.N, bb);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = fmaf(rr, v[j], fmaf(-rm, w[j], bb[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= rr;
+      }
       uint32_t ap[8];
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
-        const float g0 = rr * v[2 * j], u0 = rr * v[2 * j + 1];
-        const float g1 = rr * v[2 * j + 2], u1 = rr * v[2 * j + 3];
+        const float g0 = v[2 * j], u0 = v[2 * j + 1];
+        const float g1 = v[2 * j + 2], u1 = v[2 * j + 3];
         const float a0 = g0 * sigmoidf_fast(g0) * u0;
         const float a1 = g1 * sigmoidf_fast(g1) * u1;
         ap[j / 2] = pack_bf16(a0, a1);
-        v[2 * j] = g0; v[2 * j + 1] = u0; v[2 * j + 2] = g1; v[2 * j + 3] = u1;
       }
       st_shared_v4(abuf + swz<32>(c.lane, 0), ap[0], ap[1], ap[2], ap[3]);
       st_shared_v4(abuf + swz<32>(c.lane, 1), ap[4], ap[5], ap[6], ap[7]);
@@ -494,6 +534,9 @@ struct EpiCEGrad {
 // Per 16-column chunk of da: one fp32 box of y (32 columns) in, one bf16 box
 // of dyhat (32 columns) out. A ring of kNL load slots keeps the y boxes of
 // the next kNL-1 chunks in flight; two store sets.
+// With LN (LayerNorm variant) two more row partials for the relocated
+// LayerNorm statistics: spart_w = sum dy w1, spart_b = sum dy b1.
+template <bool LN>
 struct EpiSwiGLUBwd {
   static constexpr int kYBufB = 4096;   // 32 rows x 32 fp32
   static constexpr int kOBufB = 2048;   // 32 rows x 32 bf16
@@ -502,7 +545,11 @@ struct EpiSwiGLUBwd {
   struct Params {
     CUtensorMap tm_y, tm_dy;
     const float* r;
-    float* spart;  // [tiles_n, M]
+    float* spart;    // [tiles_n, M]
+    const float* w1;  // LN only, [2N]
+    const float* b1;  // LN only, [2N]
+    float* spart_w;   // LN only, [tiles_n, M]
+    float* spart_b;   // LN only, [tiles_n, M]
   };
   static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int ycol,
                                                int m0) {
@@ -520,7 +567,7 @@ struct EpiSwiGLUBwd {
     constexpr int NCH = BN / 16;
     const int row = m0 + 32 * c.q + c.lane;
     const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
-    float ss = 0.f;
+    float ss = 0.f, sw = 0.f, sb = 0.f;
     for (int ch = 0; ch < NCH; ++ch) {
       const int slot = c.cnt % kNL;
       const uint32_t ybuf = c.buf + slot * kYBufB;
@@ -529,6 +576,11 @@ struct EpiSwiGLUBwd {
       if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, 2 * (n0 + (ch + kNL - 1) * 16), m0);
       float da[16];
       tmem_ld16(taddr + ch * 16, da);
+      float w[32], bb[32];
+      if constexpr (LN) {
+        load_nvec32f(p.w1, 2 * (n0 + ch * 16), 2 * g.N, w);
+        load_nvec32f(p.b1, 2 * (n0 + ch * 16), 2 * g.N, bb);
+      }
       if (!c.wait(slot, 12)) return false;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {  // output chunk k = pairs 4k .. 4k+3
@@ -547,6 +599,11 @@ struct EpiSwiGLUBwd {
           const float dg = d * uu * sg * (1.0f + gg * (1.0f - sg));
           const float du = d * gg * sg;
           ss = fmaf(dg, gg, fmaf(du, uu, ss));
+          if constexpr (LN) {
+            const int q2 = 2 * (4 * k + t);
+            sw = fmaf(dg, w[q2], fmaf(du, w[q2 + 1], sw));
+            sb = fmaf(dg, bb[q2], fmaf(du, bb[q2 + 1], sb));
+          }
           outw[t] = pack_bf16(rr * dg, rr * du);
         }
         st_shared_v4(obuf + swz<64>(c.lane, k), outw[0], outw[1], outw[2], outw[3]);
@@ -559,7 +616,13 @@ struct EpiSwiGLUBwd {
       }
       ++c.cnt;
     }
-    if (row < g.M) p.spart[(size_t)nb * g.M + row] = ss;
+    if (row < g.M) {
+      p.spart[(size_t)nb * g.M + row] = ss;
+      if constexpr (LN) {
+        p.spart_w[(size_t)nb * g.M + row] = sw;
+        p.spart_b[(size_t)nb * g.M + row] = sb;
+      }
+    }
     return true;
   }
 };
@@ -568,21 +631,33 @@ struct EpiSwiGLUBwd {
 // RMSNorm backward fused into the GEMM P = dyhat W1^T ("Reading notes on
 // CODA", s3): P = r dh2, so
 //   dh = gamma P - r^2 s h (+ dres) (stored) ; dgamma partial = sum_rows P h
+// With LN (LayerNorm variant; s_a, s_b the two relocated statistics):
+//   dh = gamma P - r s_a - r^2 s_b (h - mu) (+ dres) ;
+//   dgamma partial = sum_rows P (h - mu) ; dbeta partial = sum_rows P / r ;
+//   optional side output hhat = (h - mu) gamma + beta / r, the operand of
+//   the W1 weight gradient (dW1 = hhat^T dyhat).
 // The column sums use a warp transpose-reduce; partials are per 32 rows.
 // A ring of kNL load slots of {h, dres} boxes runs kNL-1 chunks ahead; two
-// store sets of dh.
+// store sets of dh (and hhat).
+template <bool LN>
 struct EpiNormBwd {
   static constexpr int kBufB = 2048;
   static constexpr int kNL = 3;
   static constexpr int kLoadB = 2 * kBufB;
-  static constexpr int kSmemPerWarp = kNL * kLoadB + 2 * kBufB;
+  static constexpr int kStoreB = (LN ? 2 : 1) * kBufB;
+  static constexpr int kSmemPerWarp = kNL * kLoadB + 2 * kStoreB;
   struct Params {
-    CUtensorMap tm_h, tm_dres, tm_dh;
+    CUtensorMap tm_h, tm_dres, tm_dh, tm_hhat;
     const __nv_bfloat16* gamma;
     const float* r;
-    const float* s;
-    float* dgpart;  // [ceil(M/32), N]
+    const float* s;                 // s (RMSNorm) or s_b (LN)
+    float* dgpart;                  // [ceil(M/32), N]
     int has_dres;
+    const float* mu;                // LN only
+    const float* sa;                // LN only
+    const __nv_bfloat16* beta;      // LN only
+    float* dbpart;                  // LN only, [ceil(M/32), N]
+    int save_hhat;                  // LN only
   };
   static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int n,
                                                int m0) {
@@ -601,15 +676,22 @@ struct EpiNormBwd {
                                               int n0, int, uint32_t taddr) {
     constexpr int NCH = BN / 32;
     const int row = m0 + 32 * c.q + c.lane;
-    const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
-    const float ss = row < g.M ? __ldg(p.s + row) : 0.f;
+    const bool live = row < g.M;
+    const float rr = live ? __ldg(p.r + row) : 0.f;
+    const float ss = live ? __ldg(p.s + row) : 0.f;
     const float k2 = rr * rr * ss;
+    float mu = 0.f, k1 = 0.f, rinv = 0.f;
+    if constexpr (LN) {
+      mu = live ? __ldg(p.mu + row) : 0.f;
+      k1 = live ? rr * __ldg(p.sa + row) : 0.f;
+      rinv = live ? 1.0f / rr : 0.f;
+    }
     const int prow = (m0 >> 5) + c.q;  // partial row (32 rows each)
     for (int ch = 0; ch < NCH; ++ch) {
       const int slot = c.cnt % kNL;
       const uint32_t hbuf = c.buf + slot * kLoadB;
       const uint32_t rbuf = hbuf + kBufB;
-      const uint32_t obuf = c.buf + kNL * kLoadB + (c.cnt & 1) * kBufB;
+      const uint32_t obuf = c.buf + kNL * kLoadB + (c.cnt & 1) * kStoreB;
       c.stores_read_but_last();
       if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, n0 + (ch + kNL - 1) * 32, m0);
       float P[32], h[32], gm[32];
@@ -617,9 +699,13 @@ struct EpiNormBwd {
       load_nvec32(p.gamma, n0 + ch * 32, g.N, gm);
       if (!c.wait(slot, 13)) return false;
       read_bf16x32(hbuf, c.lane, h);
+      if constexpr (LN) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) h[j] -= mu;  // h - mu from here on
+      }
       float dh[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) dh[j] = gm[j] * P[j] - k2 * h[j];
+      for (int j = 0; j < 32; ++j) dh[j] = gm[j] * P[j] - k2 * h[j] - k1;
       if (p.has_dres) {
         if (!c.wait(kNL + slot, 14)) return false;
         float rz[32];
@@ -628,17 +714,36 @@ struct EpiNormBwd {
         for (int j = 0; j < 32; ++j) dh[j] += rz[j];
       }
       stage_bf16x32(obuf, c.lane, dh);
+      if constexpr (LN) {
+        if (p.save_hhat) {
+          float bt[32];
+          load_nvec32(p.beta, n0 + ch * 32, g.N, bt);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dh[j] = fmaf(h[j], gm[j], bt[j] * rinv);
+          stage_bf16x32(obuf + kBufB, c.lane, dh);
+        }
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
         c.store(&p.tm_dh, obuf, n0 + ch * 32, m0 + 32 * c.q);
+        if constexpr (LN) {
+          if (p.save_hhat) c.store(&p.tm_hhat, obuf + kBufB, n0 + ch * 32, m0 + 32 * c.q);
+        }
         bulk_commit();
+      }
+      const int col = n0 + ch * 32 + c.lane;
+      const bool wr = col < g.N && m0 + 32 * c.q < g.M;
+      if constexpr (LN) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dh[j] = P[j] * rinv;
+        const float bsum = warp_colsum32(dh, c.lane);
+        if (wr) p.dbpart[(size_t)prow * g.N + col] = bsum;
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) P[j] *= h[j];
       const float colsum = warp_colsum32(P, c.lane);
-      const int col = n0 + ch * 32 + c.lane;
-      if (col < g.N && m0 + 32 * c.q < g.M) p.dgpart[(size_t)prow * g.N + col] = colsum;
+      if (wr) p.dgpart[(size_t)prow * g.N + col] = colsum;
       ++c.cnt;
     }
     return true;

@@ -1,34 +1,54 @@
 // Reverse-fused backward GEMM-plus-epilogue kernels. Both multiply an
 // activation gradient by a transposed weight: A K-major [M, K], B K-major
-// (the weight stored [N, K]).
+// (the weight stored [N, K]). Each has an RMSNorm and a LayerNorm form.
 #include "core/launch.cuh"
 
 namespace coda {
 
-cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
-  using E = EpiSwiGLUBwd;
+template <bool LN>
+static cudaError_t swiglu_bwd_impl(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
+  using E = EpiSwiGLUBwd<LN>;
   using T = Gemm2Traits<kTileN, false, false, E>;
-  E::Params p;
+  typename E::Params p{};
   p.tm_y = a.tm_y;
   p.tm_dy = a.tm_dy;
   p.r = a.r;
   p.spart = a.spart;
+  p.w1 = a.w1;
+  p.b1 = a.b1;
+  p.spart_w = a.spart_w;
+  p.spart_b = a.spart_b;
   return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
-cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc) {
-  using E = EpiNormBwd;
+cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
+  return a.ln ? swiglu_bwd_impl<true>(a, lc) : swiglu_bwd_impl<false>(a, lc);
+}
+
+template <bool LN>
+static cudaError_t norm_bwd_impl(const NormBwdArgs& a, const LaunchCtx& lc) {
+  using E = EpiNormBwd<LN>;
   using T = Gemm2Traits<kTileN, false, false, E>;
-  E::Params p;
+  typename E::Params p{};
   p.tm_h = a.tm_h;
   p.tm_dres = a.tm_dres;
   p.tm_dh = a.tm_dh;
+  p.tm_hhat = a.tm_hhat;
   p.gamma = a.gamma;
   p.r = a.r;
   p.s = a.s;
   p.dgpart = a.dgpart;
   p.has_dres = a.has_dres;
+  p.mu = a.mu;
+  p.sa = a.sa;
+  p.beta = a.beta;
+  p.dbpart = a.dbpart;
+  p.save_hhat = a.save_hhat;
   return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+}
+
+cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc) {
+  return a.ln ? norm_bwd_impl<true>(a, lc) : norm_bwd_impl<false>(a, lc);
 }
 
 }  // namespace coda

@@ -5,33 +5,47 @@
 
 namespace coda {
 
-cudaError_t launch_resid_norm_stats(const ResidNormStatsArgs& a, const LaunchCtx& lc) {
-  using E = EpiResidNormStats;
+template <bool LN>
+static cudaError_t resid_norm_stats_impl(const ResidNormStatsArgs& a, const LaunchCtx& lc) {
+  using E = EpiResidNormStats<LN>;
   using T = Gemm2Traits<kTileN, false, true, E>;
-  E::Params p;
+  typename E::Params p{};
   p.tm_z = a.tm_z;
   p.tm_h = a.tm_h;
   p.tm_hg = a.tm_hg;
   p.gamma = a.gamma;
   p.part = a.part;
+  p.part2 = a.part2;
   return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
-cudaError_t launch_rowscale_swiglu(const RowScaleSwiGLUArgs& a, const LaunchCtx& lc) {
-  using E = EpiRowScaleSwiGLU;
+cudaError_t launch_resid_norm_stats(const ResidNormStatsArgs& a, const LaunchCtx& lc) {
+  return a.ln ? resid_norm_stats_impl<true>(a, lc) : resid_norm_stats_impl<false>(a, lc);
+}
+
+template <bool LN>
+static cudaError_t rowscale_swiglu_impl(const RowScaleSwiGLUArgs& a, const LaunchCtx& lc) {
+  using E = EpiRowScaleSwiGLU<LN>;
   using T = Gemm2Traits<kTileN, false, true, E>;
-  E::Params p;
+  typename E::Params p{};
   p.tm_a = a.tm_a;
   p.tm_y = a.tm_y;
   p.r = a.r;
   p.save_y = a.save_y;
+  p.mu = a.mu;
+  p.w1 = a.w1;
+  p.b1 = a.b1;
   return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
+}
+
+cudaError_t launch_rowscale_swiglu(const RowScaleSwiGLUArgs& a, const LaunchCtx& lc) {
+  return a.ln ? rowscale_swiglu_impl<true>(a, lc) : rowscale_swiglu_impl<false>(a, lc);
 }
 
 cudaError_t launch_rope(const RopeArgs& a, const LaunchCtx& lc) {
   using E = EpiRope;
   using T = Gemm2Traits<kTileN, false, true, E>;
-  E::Params p;
+  E::Params p{};
   p.tm_out = a.tm_out;
   p.tm_save = a.tm_save;
   p.save = a.save;
@@ -46,7 +60,7 @@ cudaError_t launch_rope(const RopeArgs& a, const LaunchCtx& lc) {
 cudaError_t launch_ce(const CEArgs& a, const LaunchCtx& lc) {
   using E = EpiCE;
   using T = Gemm2Traits<kTileN, false, true, E>;
-  E::Params p;
+  E::Params p{};
   p.targets = a.targets;
   p.part = a.part;
   p.tlogit = a.tlogit;
@@ -56,7 +70,7 @@ cudaError_t launch_ce(const CEArgs& a, const LaunchCtx& lc) {
 cudaError_t launch_ce_grad(const CEGradArgs& a, const LaunchCtx& lc) {
   using E = EpiCEGrad;
   using T = Gemm2Traits<kTileN, false, true, E>;
-  E::Params p;
+  E::Params p{};
   p.tm_g = a.tm_g;
   p.targets = a.targets;
   p.lse = a.lse;

@@ -8,7 +8,7 @@ template <bool AMN, bool BMN, bool F32, bool R, bool Q>
 static cudaError_t plain_impl(const PlainArgs& a, const LaunchCtx& lc) {
   using E = EpiPlain<F32, R, Q>;
   using T = Gemm2Traits<kTileN, AMN, BMN, E>;
-  typename E::Params p;
+  typename E::Params p{};
   p.tm_c = a.tmC;
   p.tm_r = a.tmR;
   p.rowsq = a.rowsq_part;

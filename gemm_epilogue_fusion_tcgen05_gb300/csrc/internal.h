@@ -32,6 +32,8 @@ struct ResidNormStatsArgs {
   const bf16* gamma;
   float* part;
   int M, N, K;
+  int ln;        // LayerNorm variant: also per-tile sums of h into part2
+  float* part2;
 };
 cudaError_t launch_resid_norm_stats(const ResidNormStatsArgs& a, const LaunchCtx& lc);
 
@@ -40,6 +42,10 @@ struct RowScaleSwiGLUArgs {
   const float* r;
   int save_y;
   int M, N, K;
+  int ln;        // LayerNorm variant: y = r acc - (r mu) w1 + b1
+  const float* mu;
+  const float* w1;
+  const float* b1;
 };
 cudaError_t launch_rowscale_swiglu(const RowScaleSwiGLUArgs& a, const LaunchCtx& lc);
 
@@ -76,17 +82,28 @@ struct SwiGLUBwdArgs {
   const float* r;
   float* spart;
   int M, N, K;
+  int ln;        // LayerNorm variant: also sum dy w1 and sum dy b1 partials
+  const float* w1;
+  const float* b1;
+  float* spart_w;
+  float* spart_b;
 };
 cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc);
 
 struct NormBwdArgs {
-  CUtensorMap tmA, tmB, tm_h, tm_dres, tm_dh;
+  CUtensorMap tmA, tmB, tm_h, tm_dres, tm_dh, tm_hhat;
   const bf16* gamma;
   const float* r;
   const float* s;
   float* dgpart;
   int has_dres;
   int M, N, K;
+  int ln;        // LayerNorm variant (s is s_b)
+  const float* mu;
+  const float* sa;
+  const bf16* beta;
+  float* dbpart;
+  int save_hhat;
 };
 cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc);
 
@@ -109,6 +126,10 @@ cudaError_t launch_rope_table(float2* cs, int seq_len, int head_dim, double thet
 cudaError_t launch_rope_bwd(const bf16* d, const float* q, const float* r, const float2* cs,
                             int seq_len, int head_dim, int n_rope, bf16* out, float* s, int M, int N,
                             float inv_d, cudaStream_t st);
+cudaError_t launch_ln_stats(const float* part_sq, const float* part_sum, int nparts, int M, float inv_d,
+                            float eps, float* r, float* mu, cudaStream_t st);
+cudaError_t launch_ln_bwd_stats(const float* spart, const float* spart_w, const float* spart_b,
+                                int nparts, int M, float inv_d, float* sa, float* sb, cudaStream_t st);
 cudaError_t launch_bounded_wait_probe(int* err, unsigned long long timeout_ns, cudaStream_t st);
 
 }  // namespace coda

@@ -265,6 +265,63 @@ coda_status_t coda_gemm_rope_bwd(const void* dqkv_rot, const float* qkv_rot, con
                                  void* dqkv_hat, float* s, int M, int N, int d,
                                  coda_stream_t stream);
 
+/* ------------------------------------------------- LayerNorm variant */
+/* The pages promise a LayerNorm composition without working it; this is the
+ * library's reading, built the same way as the RMSNorm path ([notes] s2-s3):
+ * with mu, r = 1/sqrt(var + eps) per row and the n-vectors w1 = gamma W1,
+ * b1 = beta W1 (fp32 [2f], e.g. two M=1 calls of coda_gemm),
+ *   ((h - mu) r gamma + beta) W1 = r (hg W1) - (r mu) w1 + b1,
+ * and the two LayerNorm-backward statistics relocate into the epilogue of
+ * the GEMM producing dy: s_a = (1/d) sum dy w1, s_b = (1/d)(sum dy y -
+ * sum dy b1). */
+
+/* GEMM 1: h = x W0 + z, hg = h * gamma (bf16), per-tile partials
+ * part_sq[t, m] = sum h^2 and part_sum[t, m] = sum h (fp32
+ * [coda_col_tiles(N), M]). Otherwise as coda_gemm_resid_norm_stats. */
+coda_status_t coda_gemm_resid_ln_stats(const void* x, const void* W0, const void* z,
+                                       const void* gamma, void* h, void* hg, float* part_sq,
+                                       float* part_sum, int M, int N, int K, coda_stream_t stream);
+
+/* mu[m] = sum_j part_sum[j, m] / d ;
+ * r[m] = 1 / sqrt(max(sum_j part_sq[j, m] / d - mu^2, 0) + eps). */
+coda_status_t coda_row_ln(const float* part_sq, const float* part_sum, int nparts, int M, int d,
+                          float eps, float* r, float* mu, coda_stream_t stream);
+
+/* GEMM 2: y = r[m] (hg W1) - (r mu)[m] w1[n] + b1[n]; a = SwiGLU(y) (bf16
+ * [M, two_f/2]); y_save (nullable) fp32 [M, two_f]. */
+coda_status_t coda_gemm_ln_rowscale_swiglu(const void* hg, const void* W1, const float* r,
+                                           const float* mu, const float* w1, const float* b1,
+                                           void* a, float* y_save, int M, int two_f, int K,
+                                           coda_stream_t stream);
+
+/* SwiGLU backward as coda_gemm_rowscale_swiglu_bwd, plus the row partials
+ * spart_w = sum dy w1 and spart_b = sum dy b1 (fp32 [coda_col_tiles(f), M]). */
+coda_status_t coda_gemm_ln_rowscale_swiglu_bwd(const void* dout, const void* W2, const float* y,
+                                               const float* r, const float* w1, const float* b1,
+                                               void* dyhat, float* spart, float* spart_w,
+                                               float* spart_b, int M, int f, int d,
+                                               coda_stream_t stream);
+
+/* s_a[m] = sum_j spart_w[j, m] / d ; s_b[m] = (sum_j spart[j, m] -
+ * sum_j spart_b[j, m]) / d. */
+coda_status_t coda_row_ln_bwd(const float* spart, const float* spart_w, const float* spart_b,
+                              int nparts, int M, int d, float* s_a, float* s_b,
+                              coda_stream_t stream);
+
+/* LayerNorm backward fused into P = dyhat W1^T:
+ *   dh = gamma P - r s_a - r^2 s_b (h - mu) (+ dresid)        (bf16 [M, d])
+ *   dgamma_part[j, n] = sum over rows 32j.. of P (h - mu)      (fp32)
+ *   dbeta_part[j, n]  = sum over rows 32j.. of P / r           (fp32)
+ *   hhat (nullable) = (h - mu) gamma + beta / r  (bf16 [M, d]): the operand
+ *   of the W1 gradient, dW1 = hhat^T dyhat.
+ * beta bf16 [d]; partial shapes [coda_row_tiles32(M), d]. */
+coda_status_t coda_gemm_resid_ln_stats_bwd(const void* dyhat, const void* W1, const void* h,
+                                           const void* gamma, const void* beta, const float* r,
+                                           const float* mu, const float* s_a, const float* s_b,
+                                           const void* dresid, void* dh, void* hhat,
+                                           float* dgamma_part, float* dbeta_part, int M, int d,
+                                           int two_f, coda_stream_t stream);
+
 /* Test hook for the bounded waits: launches one tiny kernel whose only wait
  * is on an mbarrier that nothing arrives at, bounded by timeout_ms. The wait
  * gives up, records CODA_ERR_TIMEOUT in the device error word and the kernel
