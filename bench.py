@@ -150,7 +150,7 @@ class Step:
         from coda_inputs import WORKLOADS, mlp_block_inputs, lmhead_inputs, block8b_inputs
         self.C = C
         self.dev = dev
-        bf, f32 = torch.bfloat16, torch.float32
+        bf, f16, f32 = torch.bfloat16, torch.float16, torch.float32
         e = lambda s, dt: torch.empty(s, dtype=dt, device=dev)
         # ---- Llama-3-1B-shaped block (forward state kept for the backward)
         s1 = WORKLOADS["llama1b_mlp_bwd"]
@@ -158,7 +158,7 @@ class Step:
         M, d, f = s1.M, s1.d, s1.f
         self.i1 = mlp_block_inputs(s1, device=dev)
         self.b1 = {"h": e((M, d), bf), "hg": e((M, d), bf), "part": e((C.col_tiles(d), M), f32),
-                   "r": e((M,), f32), "a": e((M, f), bf), "y": e((M, 2 * f), f32),
+                   "r": e((M,), f32), "a": e((M, f), bf), "y": e((M, 2 * f), f16),
                    "out": e((M, d), bf), "dyhat": e((M, 2 * f), bf),
                    "spart": e((C.col_tiles(f), M), f32), "s": e((M,), f32), "dh": e((M, d), bf),
                    "dgpart": e((C.row_tiles32(M), d), f32), "dgamma": e((d,), f32),
@@ -181,9 +181,9 @@ class Step:
             M4, d4, f4, n4 = s4.M, s4.d, s4.f, s4.n_qkv
             self.b4 = {"h": e((M4, d4), bf), "hg": e((M4, d4), bf),
                        "part": e((C.col_tiles(d4), M4), f32), "r": e((M4,), f32),
-                       "a": e((M4, f4), bf), "y": e((M4, 2 * f4), f32), "out": e((M4, d4), bf),
+                       "a": e((M4, f4), bf), "y": e((M4, 2 * f4), f16), "out": e((M4, d4), bf),
                        "outg": e((M4, d4), bf), "part1": e((C.col_tiles(d4), M4), f32),
-                       "r1": e((M4,), f32), "qkv": e((M4, n4), bf), "qkv32": e((M4, n4), f32),
+                       "r1": e((M4,), f32), "qkv": e((M4, n4), bf), "qkv_save": e((M4, n4), f16),
                        "dqh": e((M4, n4), bf),
                        "s1": e((M4,), f32), "dout": e((M4, d4), bf),
                        "dgp1": e((C.row_tiles32(M4), d4), f32), "dgamma1": e((d4,), f32),
@@ -241,9 +241,9 @@ class Step:
             add("8b.row_rms1", 0, lambda: C.coda_row_rms(b4["part1"], b4["r1"], d4, 1e-6))
             add("8b.gemm_rope", 2 * M4 * d4 * n4,
                 lambda: C.coda_gemm_rope(b4["outg"], i4["Wqkv"], b4["r1"], cs, sl, hd, nr, b4["qkv"],
-                                         b4["qkv32"]))
+                                         b4["qkv_save"]))
             add("8b.rope_bwd", 0,
-                lambda: C.coda_gemm_rope_bwd(i4["dqkv"], b4["qkv32"], b4["r1"], cs, sl, hd, nr,
+                lambda: C.coda_gemm_rope_bwd(i4["dqkv"], b4["qkv_save"], b4["r1"], cs, sl, hd, nr,
                                              b4["dqh"], b4["s1"], d4))
             add("8b.gemm_resid_norm_stats_bwd(Wqkv)", 2 * M4 * n4 * d4,
                 lambda: C.coda_gemm_resid_norm_stats_bwd(b4["dqh"], i4["Wqkv"], b4["out"],
@@ -478,9 +478,56 @@ def next_rows(step, flush, reps=5):
     ms = sorted(ts)[len(ts) // 2]
     fl = 3 * 2.0 * s2.M * s2.d * s2.V
     chunk = min(4096, (s2.V + 255) // 256 * 256)
-    return {"lmhead_ce_bwd": {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+    rows = {"lmhead_ce_bwd": {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
                               "tokens_per_s": round(s2.M / (ms * 1e-3), 1),
                               "launches": 3 * ((s2.V + chunk - 1) // chunk)}}
+    rows.update(layernorm_row(step, flush, reps))
+    return rows
+
+
+def _median_ms(fn, flush, reps):
+    fn()
+    torch.cuda.synchronize()
+    ts = []
+    for i in range(reps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return sorted(ts)[len(ts) // 2]
+
+
+def layernorm_row(step, flush, reps=5):
+    """The LayerNorm variant of the MLP block, forward + backward, on the
+    Llama-1B MLP shape (M=8192, d=2048, f=8192), timed beside the RMSNorm
+    block run the same way (block-level calls, buffers from torch's caching
+    allocator). GEMM FLOPs: forward 2M(d^2 + 3df), backward twice that."""
+    from gemm_epilogue_fusion_tcgen05_gb300 import blocks
+    from coda_inputs import BlockShape, ln_block_inputs
+    s1 = step.s1
+    sh = BlockShape("llama1b_ln_mlp", M=s1.M, d=s1.d, f=s1.f, seed=7)
+    g = ln_block_inputs(sh, device=step.dev)
+
+    def ln():
+        fw = blocks.ln_mlp_block_fwd(g["x"], g["z"], g["W0"], g["W1"], g["W2"], g["gamma"],
+                                     g["beta"])
+        blocks.ln_mlp_block_bwd(fw, g["x"], g["W0"], g["W1"], g["W2"], g["gamma"], g["beta"],
+                                g["dout"])
+
+    def rms():
+        fw = blocks.mlp_block_fwd(g["x"], g["z"], g["W0"], g["W1"], g["W2"], g["gamma"])
+        blocks.mlp_block_bwd(fw, g["x"], g["W0"], g["W1"], g["W2"], g["gamma"], g["dout"])
+
+    ms_ln = _median_ms(ln, flush, reps)
+    ms_rms = _median_ms(rms, flush, reps)
+    fl = 3 * 2.0 * sh.M * (sh.d * sh.d + 3 * sh.d * sh.f)
+    return {"layernorm_mlp_fwd_bwd": {
+        "ms": round(ms_ln, 4), "tflops": round(fl / (ms_ln * 1e-3) / 1e12, 2),
+        "rmsnorm_same_calls_ms": round(ms_rms, 4),
+        "ratio_to_rmsnorm": round(ms_ln / ms_rms, 3), "launches": 15}}
 
 
 # ------------------------------------------------------------------ unfused GPU reference

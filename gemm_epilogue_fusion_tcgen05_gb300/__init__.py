@@ -25,9 +25,10 @@ __all__ = [
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoda.so")
 
-CODA_OK, CODA_ERR_INVALID_VALUE, CODA_ERR_UNSUPPORTED, CODA_ERR_LAUNCH, CODA_ERR_TIMEOUT = range(5)
+(CODA_OK, CODA_ERR_INVALID_VALUE, CODA_ERR_UNSUPPORTED, CODA_ERR_LAUNCH, CODA_ERR_TIMEOUT,
+ CODA_ERR_RANGE) = range(6)
 _STATUS = {0: "CODA_OK", 1: "CODA_ERR_INVALID_VALUE", 2: "CODA_ERR_UNSUPPORTED",
-           3: "CODA_ERR_LAUNCH", 4: "CODA_ERR_TIMEOUT"}
+           3: "CODA_ERR_LAUNCH", 4: "CODA_ERR_TIMEOUT", 5: "CODA_ERR_RANGE"}
 
 _P, _I, _F, _D, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_size_t
 
@@ -119,7 +120,7 @@ def _req(t: torch.Tensor, dtype, name: str, ndim: int = 2):
         raise ValueError(f"{name}: must be contiguous")
 
 
-bf16, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+bf16, f16, f32, i32 = torch.bfloat16, torch.float16, torch.float32, torch.int32
 
 
 def col_tiles(N: int) -> int:
@@ -194,7 +195,7 @@ def coda_gemm_rowscale_swiglu(hg, W1, r, a, y_save=None, stream=None):
     _req(a, bf16, "a")
     _req(r, f32, "r", 1)
     if y_save is not None:
-        _req(y_save, f32, "y_save")
+        _req(y_save, f16, "y_save")
     _check(lib().coda_gemm_rowscale_swiglu(_ptr(hg), _ptr(W1), _ptr(r), _ptr(a), _ptr(y_save),
                                            M, two_f, K, _stream(stream)))
 
@@ -205,16 +206,16 @@ def coda_rope_table(cos_sin, seq_len: int, head_dim: int, theta: float, stream=N
 
 
 def coda_gemm_rope(A, W, r, cos_sin, seq_len: int, head_dim: int, n_rope_cols: int, out,
-                   out_f32=None, stream=None):
+                   out_f16=None, stream=None):
     M, K = A.shape
     N = W.shape[1]
     _req(A, bf16, "A")
     _req(W, bf16, "W")
     _req(out, bf16, "out")
-    if out_f32 is not None:
-        _req(out_f32, f32, "out_f32")
+    if out_f16 is not None:
+        _req(out_f16, f16, "out_f16")
     _check(lib().coda_gemm_rope(_ptr(A), _ptr(W), _ptr(r), _ptr(cos_sin), seq_len, head_dim,
-                                n_rope_cols, _ptr(out), _ptr(out_f32), M, N, K, _stream(stream)))
+                                n_rope_cols, _ptr(out), _ptr(out_f16), M, N, K, _stream(stream)))
 
 
 def coda_lmhead_ce_workspace_size(M: int, V: int) -> int:
@@ -283,7 +284,7 @@ def coda_gemm_ln_rowscale_swiglu(hg, W1, r, mu, w1, b1, a, y_save=None, stream=N
     for t, n in ((r, "r"), (mu, "mu"), (w1, "w1"), (b1, "b1")):
         _req(t, f32, n, 1)
     if y_save is not None:
-        _req(y_save, f32, "y_save")
+        _req(y_save, f16, "y_save")
     _check(lib().coda_gemm_ln_rowscale_swiglu(_ptr(hg), _ptr(W1), _ptr(r), _ptr(mu), _ptr(w1),
                                               _ptr(b1), _ptr(a), _ptr(y_save), M, two_f, K,
                                               _stream(stream)))
@@ -293,7 +294,7 @@ def coda_gemm_ln_rowscale_swiglu_bwd(dout, W2, y, r, w1, b1, dyhat, spart, spart
                                      stream=None):
     M, d = dout.shape
     f = W2.shape[0]
-    _req(y, f32, "y")
+    _req(y, f16, "y")
     _check(lib().coda_gemm_ln_rowscale_swiglu_bwd(_ptr(dout), _ptr(W2), _ptr(y), _ptr(r),
                                                   _ptr(w1), _ptr(b1), _ptr(dyhat), _ptr(spart),
                                                   _ptr(spart_w), _ptr(spart_b), M, f, d,
@@ -338,7 +339,7 @@ def coda_gemm_rowscale_swiglu_bwd(dout, W2, y, r, dyhat, spart, stream=None):
     f = W2.shape[0]
     for t, n in ((dout, "dout"), (W2, "W2"), (dyhat, "dyhat")):
         _req(t, bf16, n)
-    _req(y, f32, "y")
+    _req(y, f16, "y")
     _req(spart, f32, "spart")
     _check(lib().coda_gemm_rowscale_swiglu_bwd(_ptr(dout), _ptr(W2), _ptr(y), _ptr(r), _ptr(dyhat),
                                                _ptr(spart), M, f, d, _stream(stream)))
@@ -369,7 +370,7 @@ def coda_gemm_rope_bwd(dqkv_rot, qkv_rot, r, cos_sin, seq_len: int, head_dim: in
                        n_rope_cols: int, dqkv_hat, s, d: int, stream=None):
     M, N = dqkv_rot.shape
     _req(dqkv_rot, bf16, "dqkv_rot")
-    _req(qkv_rot, f32, "qkv_rot")
+    _req(qkv_rot, f16, "qkv_rot")
     _check(lib().coda_gemm_rope_bwd(_ptr(dqkv_rot), _ptr(qkv_rot), _ptr(r), _ptr(cos_sin), seq_len,
                                     head_dim, n_rope_cols, _ptr(dqkv_hat), _ptr(s), M, N, d,
                                     _stream(stream)))

@@ -23,7 +23,7 @@ from . import (coda_col_reduce, coda_gemm, coda_gemm_resid_norm_stats,
                coda_rope_table, coda_row_rms, coda_row_rms_bwd,
                col_tiles, row_tiles32)
 
-bf16, f32 = torch.bfloat16, torch.float32
+bf16, f16, f32 = torch.bfloat16, torch.float16, torch.float32
 
 
 def _e(shape, dtype, dev):
@@ -43,7 +43,7 @@ def mlp_block_fwd(x, z, W0, W1, W2, gamma, eps: float = 1e-6, save_y: bool = Tru
     part = b.get("part") if "part" in b else _e((col_tiles(d), M), f32, dev)
     r = b.get("r") if "r" in b else _e((M,), f32, dev)
     a = b.get("a") if "a" in b else _e((M, two_f // 2), bf16, dev)
-    y = (b.get("y") if "y" in b else _e((M, two_f), f32, dev)) if save_y else None
+    y = (b.get("y") if "y" in b else _e((M, two_f), f16, dev)) if save_y else None
     out = b.get("out") if "out" in b else _e((M, d), bf16, dev)
     coda_gemm_resid_norm_stats(x, W0, z, gamma, h, hg, part)
     coda_row_rms(part, r, d, eps)
@@ -99,7 +99,7 @@ def ln_mlp_block_fwd(x, z, W0, W1, W2, gamma, beta, eps: float = 1e-6) -> Dict[s
     psq, psum = _e((col_tiles(d), M), f32, dev), _e((col_tiles(d), M), f32, dev)
     r, mu = _e((M,), f32, dev), _e((M,), f32, dev)
     w1, b1 = _e((1, two_f), f32, dev), _e((1, two_f), f32, dev)
-    a, y = _e((M, two_f // 2), bf16, dev), _e((M, two_f), f32, dev)
+    a, y = _e((M, two_f // 2), bf16, dev), _e((M, two_f), f16, dev)
     out = _e((M, d), bf16, dev)
     coda_gemm(gamma.view(1, d), W1, w1)
     coda_gemm(beta.view(1, d), W1, b1)
@@ -192,20 +192,20 @@ def block8b_fwd(inp: Dict[str, torch.Tensor], seq_len: int, head_dim: int, n_rop
     part = _e((col_tiles(d), M), f32, dev)
     r = _e((M,), f32, dev)
     a = _e((M, two_f // 2), bf16, dev)
-    y = _e((M, two_f), f32, dev)
+    y = _e((M, two_f), f16, dev)
     out, outg = _e((M, d), bf16, dev), _e((M, d), bf16, dev)
     part1 = _e((col_tiles(d), M), f32, dev)
     r1 = _e((M,), f32, dev)
     qkv = _e((M, nq), bf16, dev)
-    qkv32 = _e((M, nq), f32, dev)
+    qkv_save = _e((M, nq), f16, dev)
     coda_gemm_resid_norm_stats(o, inp["Wo"], z, inp["gamma2"], h, hg, part)
     coda_row_rms(part, r, d, eps)
     coda_gemm_rowscale_swiglu(hg, inp["W1"], r, a, y)
     coda_gemm_resid_norm_stats(a, inp["W2"], h, inp["gamma1"], out, outg, part1)
     coda_row_rms(part1, r1, d, eps)
-    coda_gemm_rope(outg, inp["Wqkv"], r1, cos_sin, seq_len, head_dim, n_rope_cols, qkv, qkv32)
+    coda_gemm_rope(outg, inp["Wqkv"], r1, cos_sin, seq_len, head_dim, n_rope_cols, qkv, qkv_save)
     return {"h": h, "hg": hg, "r": r, "a": a, "y": y, "out": out, "outg": outg, "r1": r1,
-            "qkv": qkv, "qkv32": qkv32}
+            "qkv": qkv, "qkv_save": qkv_save}
 
 
 def block8b_bwd(fwd: Dict[str, torch.Tensor], inp: Dict[str, torch.Tensor], seq_len: int,
@@ -220,7 +220,7 @@ def block8b_bwd(fwd: Dict[str, torch.Tensor], inp: Dict[str, torch.Tensor], seq_
     dev = o.device
     dqh = _e((M, nq), bf16, dev)
     s1 = _e((M,), f32, dev)
-    coda_gemm_rope_bwd(inp["dqkv"], fwd["qkv32"], fwd["r1"], cos_sin, seq_len, head_dim,
+    coda_gemm_rope_bwd(inp["dqkv"], fwd["qkv_save"], fwd["r1"], cos_sin, seq_len, head_dim,
                        n_rope_cols, dqh, s1, d)
     dout = _e((M, d), bf16, dev)
     dgp1 = _e((row_tiles32(M), d), f32, dev)

@@ -136,6 +136,10 @@ bool map_bf16_64(CUtensorMap* m, const void* p, int rows, int cols, int ld) {
   return tmap2d(m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, ld, 64, 32,
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
+bool map_f16_32(CUtensorMap* m, const void* p, int rows, int cols, int ld) {
+  return tmap2d(m, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, cols, rows, ld, 32, 32,
+                CU_TENSOR_MAP_SWIZZLE_64B);
+}
 bool map_f32_32(CUtensorMap* m, const void* p, int rows, int cols, int ld) {
   return tmap2d(m, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cols, rows, ld, 32, 32,
                 CU_TENSOR_MAP_SWIZZLE_128B);
@@ -200,6 +204,9 @@ coda_status_t coda_get_device_error(coda_stream_t stream) {
   const int code = v & 0xff, where = v >> 8;
   if (code == kErrTimeout)
     return fail(CODA_ERR_TIMEOUT, "a bounded wait in a kernel ran out (site %d)", where);
+  if (code == kErrRange)
+    return fail(CODA_ERR_RANGE, "a value saved in fp16 was outside the fp16 range (site %d)",
+                where);
   return fail(CODA_ERR_INVALID_VALUE, "device-side invalid value (site %d)", where);
 }
 
@@ -299,7 +306,7 @@ coda_status_t coda_gemm_rowscale_swiglu(const void* hg, const void* W1, const fl
   CHECK_MAP(map_a(&p.tmA, hg, K, 0, M, K));
   CHECK_MAP(map_b(&p.tmB, W1, two_f, 0, two_f, K));
   CHECK_MAP(map_bf16_16(&p.tm_a, a, M, two_f / 2, two_f / 2));
-  if (y_save) CHECK_MAP(map_f32_32(&p.tm_y, y_save, M, two_f, two_f));
+  if (y_save) CHECK_MAP(map_f16_32(&p.tm_y, y_save, M, two_f, two_f));
   else p.tm_y = p.tm_a;  // unused
   p.r = r;
   p.save_y = y_save != nullptr;
@@ -310,14 +317,14 @@ coda_status_t coda_gemm_rowscale_swiglu(const void* hg, const void* W1, const fl
 }
 
 coda_status_t coda_gemm_rope(const void* A, const void* W, const float* r, const float* cos_sin,
-                             int seq_len, int head_dim, int n_rope_cols, void* out, float* out_f32,
+                             int seq_len, int head_dim, int n_rope_cols, void* out, void* out_f16,
                              int M, int N, int K, coda_stream_t stream) {
   CHECK_PTR(A);
   CHECK_PTR(W);
   CHECK_OPT_PTR(r);
   CHECK_PTR(cos_sin);
   CHECK_PTR(out);
-  CHECK_OPT_PTR(out_f32);
+  CHECK_OPT_PTR(out_f16);
   CHECK(M > 0 && N > 0 && K > 0 && M < kMaxDim && N < kMaxDim && K < kMaxDim,
         "coda_gemm_rope: bad sizes");
   CHECK(N % 8 == 0 && K % 8 == 0, "coda_gemm_rope: N and K must be multiples of 8");
@@ -329,9 +336,9 @@ coda_status_t coda_gemm_rope(const void* A, const void* W, const float* r, const
   CHECK_MAP(map_a(&p.tmA, A, K, 0, M, K));
   CHECK_MAP(map_b(&p.tmB, W, N, 0, N, K));
   CHECK_MAP(map_bf16_32(&p.tm_out, out, M, N, N));
-  if (out_f32) CHECK_MAP(map_f32_32(&p.tm_save, out_f32, M, N, N));
+  if (out_f16) CHECK_MAP(map_f16_32(&p.tm_save, out_f16, M, N, N));
   else p.tm_save = p.tm_out;  // unused
-  p.save = out_f32 != nullptr;
+  p.save = out_f16 != nullptr;
   p.r = r;
   p.cs = reinterpret_cast<const float2*>(cos_sin);
   p.seq_len = seq_len;
@@ -497,7 +504,7 @@ coda_status_t coda_gemm_rowscale_swiglu_bwd(const void* dout, const void* W2, co
   SwiGLUBwdArgs p{};
   CHECK_MAP(map_a(&p.tmA, dout, d, 0, M, d));
   CHECK_MAP(map_b(&p.tmB, W2, d, 1, f, d));  // B[k, n] = W2[n, k]
-  CHECK_MAP(map_f32_32(&p.tm_y, y, M, 2 * f, 2 * f));
+  CHECK_MAP(map_f16_32(&p.tm_y, y, M, 2 * f, 2 * f));
   CHECK_MAP(map_bf16_32(&p.tm_dy, dyhat, M, 2 * f, 2 * f));
   p.r = r;
   p.spart = spart;
@@ -562,7 +569,7 @@ coda_status_t coda_col_reduce(const float* part, int nparts, int N, float* out,
   return from_cuda(launch_col_reduce(part, nparts, N, out, lc.stream), "coda_col_reduce launch");
 }
 
-coda_status_t coda_gemm_rope_bwd(const void* dqkv_rot, const float* qkv_rot, const float* r,
+coda_status_t coda_gemm_rope_bwd(const void* dqkv_rot, const void* qkv_rot, const float* r,
                                  const float* cos_sin, int seq_len, int head_dim, int n_rope_cols,
                                  void* dqkv_hat, float* s, int M, int N, int d,
                                  coda_stream_t stream) {
@@ -577,7 +584,8 @@ coda_status_t coda_gemm_rope_bwd(const void* dqkv_rot, const float* qkv_rot, con
   CHECK(n_rope_cols >= 0 && n_rope_cols <= N && n_rope_cols % head_dim == 0,
         "coda_gemm_rope_bwd: n_rope_cols must be a multiple of head_dim and <= N");
   TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
-  return from_cuda(launch_rope_bwd(static_cast<const bf16*>(dqkv_rot), qkv_rot, r,
+  return from_cuda(launch_rope_bwd(static_cast<const bf16*>(dqkv_rot),
+                                   static_cast<const __half*>(qkv_rot), r,
                                    reinterpret_cast<const float2*>(cos_sin), seq_len, head_dim,
                                    n_rope_cols, static_cast<bf16*>(dqkv_hat), s, M, N,
                                    1.0f / (float)d, lc.stream),
@@ -633,7 +641,7 @@ coda_status_t coda_row_ln(const float* part_sq, const float* part_sum, int npart
 
 coda_status_t coda_gemm_ln_rowscale_swiglu(const void* hg, const void* W1, const float* r,
                                            const float* mu, const float* w1, const float* b1,
-                                           void* a, float* y_save, int M, int two_f, int K,
+                                           void* a, void* y_save, int M, int two_f, int K,
                                            coda_stream_t stream) {
   CHECK_PTR(hg);
   CHECK_PTR(W1);
@@ -652,7 +660,7 @@ coda_status_t coda_gemm_ln_rowscale_swiglu(const void* hg, const void* W1, const
   CHECK_MAP(map_a(&p.tmA, hg, K, 0, M, K));
   CHECK_MAP(map_b(&p.tmB, W1, two_f, 0, two_f, K));
   CHECK_MAP(map_bf16_16(&p.tm_a, a, M, two_f / 2, two_f / 2));
-  if (y_save) CHECK_MAP(map_f32_32(&p.tm_y, y_save, M, two_f, two_f));
+  if (y_save) CHECK_MAP(map_f16_32(&p.tm_y, y_save, M, two_f, two_f));
   else p.tm_y = p.tm_a;  // unused
   p.r = r;
   p.mu = mu;
@@ -666,7 +674,7 @@ coda_status_t coda_gemm_ln_rowscale_swiglu(const void* hg, const void* W1, const
   return from_cuda(launch_rowscale_swiglu(p, lc), "coda_gemm_ln_rowscale_swiglu launch");
 }
 
-coda_status_t coda_gemm_ln_rowscale_swiglu_bwd(const void* dout, const void* W2, const float* y,
+coda_status_t coda_gemm_ln_rowscale_swiglu_bwd(const void* dout, const void* W2, const void* y,
                                                const float* r, const float* w1, const float* b1,
                                                void* dyhat, float* spart, float* spart_w,
                                                float* spart_b, int M, int f, int d,
@@ -689,7 +697,7 @@ coda_status_t coda_gemm_ln_rowscale_swiglu_bwd(const void* dout, const void* W2,
   SwiGLUBwdArgs p{};
   CHECK_MAP(map_a(&p.tmA, dout, d, 0, M, d));
   CHECK_MAP(map_b(&p.tmB, W2, d, 1, f, d));
-  CHECK_MAP(map_f32_32(&p.tm_y, y, M, 2 * f, 2 * f));
+  CHECK_MAP(map_f16_32(&p.tm_y, y, M, 2 * f, 2 * f));
   CHECK_MAP(map_bf16_32(&p.tm_dy, dyhat, M, 2 * f, 2 * f));
   p.r = r;
   p.spart = spart;

@@ -122,9 +122,9 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, int seq_len, int head
 // part of this library, so this pairwise map runs on its own):
 //   dhat = r[m] * R(pos)^T d   (pairs of the q and k columns; v unrotated)
 //   s[m] = inv_d * sum_n d[m, n] * q[m, n]   (rotation keeps dot products;
-//          q is the fp32 copy of the forward output kept for this purpose)
+//          q is the fp16 copy of the forward output kept for this purpose)
 // One block of 128 threads per row; vectors of 8 columns (4 pairs).
-__global__ void rope_bwd_kernel(const __nv_bfloat16* __restrict__ d, const float* __restrict__ q,
+__global__ void rope_bwd_kernel(const __nv_bfloat16* __restrict__ d, const __half* __restrict__ q,
                                 const float* __restrict__ r, const float2* __restrict__ cs,
                                 int seq_len, int head_dim, int n_rope, __nv_bfloat16* __restrict__ out,
                                 float* __restrict__ s, int M, int N, float inv_d) {
@@ -133,16 +133,23 @@ __global__ void rope_bwd_kernel(const __nv_bfloat16* __restrict__ d, const float
   const float rr = r ? __ldg(r + m) : 1.f;
   const int pos = m % seq_len;
   const uint4* drow = reinterpret_cast<const uint4*>(d + (size_t)m * N);
-  const float4* qrow = reinterpret_cast<const float4*>(q + (size_t)m * N);
+  const uint4* qrow = reinterpret_cast<const uint4*>(q + (size_t)m * N);
   uint4* orow = reinterpret_cast<uint4*>(out + (size_t)m * N);
   const float2* csr = cs + (size_t)pos * (head_dim / 2);
   float acc = 0.f;
   const int nvec = N / 8;
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     const uint4 du = __ldg(drow + v);
-    const float4 q0 = __ldg(qrow + 2 * v), q1 = __ldg(qrow + 2 * v + 1);
+    const uint4 qu = __ldg(qrow + v);
     const uint32_t dw[4] = {du.x, du.y, du.z, du.w};
-    const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t qw[4] = {qu.x, qu.y, qu.z, qu.w};
+    float qv[8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qw[t]));
+      qv[2 * t] = f.x;
+      qv[2 * t + 1] = f.y;
+    }
     const int col = v * 8;
     const bool rot = col < n_rope;
     const int i0 = (col % head_dim) / 2;
@@ -254,7 +261,7 @@ cudaError_t launch_rope_table(float2* cs, int seq_len, int head_dim, double thet
   rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(cs, seq_len, head_dim, theta);
   return cudaGetLastError();
 }
-cudaError_t launch_rope_bwd(const __nv_bfloat16* d, const float* q, const float* r,
+cudaError_t launch_rope_bwd(const __nv_bfloat16* d, const __half* q, const float* r,
                             const float2* cs, int seq_len, int head_dim, int n_rope,
                             __nv_bfloat16* out, float* s, int M, int N, float inv_d, cudaStream_t st) {
   rope_bwd_kernel<<<M, 128, 0, st>>>(d, q, r, cs, seq_len, head_dim, n_rope, out, s, M, N, inv_d);

@@ -75,6 +75,38 @@ __device__ __forceinline__ void read_bf16x32(uint32_t buf, int lane, float (&v)[
   for (int k = 0; k < 4; ++k) unpack8(ld_shared_v4(buf + swz<64>(lane, k)), &v[8 * k]);
 }
 
+// fp16 pair packing (round to nearest); the low half holds `lo`.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_f16(uint32_t u) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+}
+
+// Saved fp16 copies: values whose magnitude rounds beyond the largest finite
+// fp16 (or that are not finite) would be stored as inf / NaN. The callers
+// raise a range error for them instead of passing them on silently.
+constexpr float kF16Limit = 65520.f;  // first magnitude that rounds to inf
+
+// Store 32 fp32 values as fp16 into row `lane` of a 64-byte-row swizzled box;
+// returns false if any of them is outside the fp16 range.
+__device__ __forceinline__ bool stage_f16x32(uint32_t buf, int lane, const float (&v)[32]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    st_shared_v4(buf + swz<64>(lane, k), pack_f16(v[8 * k], v[8 * k + 1]),
+                 pack_f16(v[8 * k + 2], v[8 * k + 3]), pack_f16(v[8 * k + 4], v[8 * k + 5]),
+                 pack_f16(v[8 * k + 6], v[8 * k + 7]));
+  // fmaxf drops NaN operands: test the values themselves for NaN as well
+  bool finite = true;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) finite &= (v[j] == v[j]);
+  return finite && amax < kF16Limit;
+}
+
 __device__ __forceinline__ float sigmoidf_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
 // Column sums of a 32 x 32 block held one row per lane: after the exchange,
@@ -264,14 +296,16 @@ struct EpiResidNormStats {
 // notes on CODA", s2: y[i,j] = r[i] h3[i,j]; pairwise activations on
 // adjacent accumulator values; pith Fig. 7 caption):
 //   y = r[m] * acc ; a_k = silu(y_2k) * y_2k+1 (bf16) ; y optionally saved in
-//   fp32 for the backward (its relocated RMSNorm statistic sums 2f products
-//   with heavy cancellation, which bf16 storage of y would dominate)
+//   fp16 for the backward (its relocated RMSNorm statistic sums 2f products
+//   with heavy cancellation: bf16's 8-bit significand would dominate it,
+//   fp16's 11 bits keep it within 1e-3 at half the bytes of fp32); a value
+//   beyond the fp16 range raises CODA_ERR_RANGE
 // With LN (LayerNorm variant): y = r[m] acc - (r mu)[m] w1[n] + b1[n], with
 // the n-vectors w1 = gamma W1 and b1 = beta W1.
 template <bool LN>
 struct EpiRowScaleSwiGLU {
   static constexpr int kABufB = 1024;  // 32 rows x 16 bf16 (32-byte rows)
-  static constexpr int kYBufB = 4096;  // 32 rows x 32 fp32 (128-byte rows)
+  static constexpr int kYBufB = 2048;  // 32 rows x 32 fp16 (64-byte rows)
   static constexpr int kSetB = kABufB + kYBufB;
   static constexpr int kSmemPerWarp = 2 * kSetB;
   struct Params {
@@ -292,6 +326,7 @@ struct EpiRowScaleSwiGLU {
     const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
     float rm = 0.f;
     if constexpr (LN) rm = row < g.M ? rr * __ldg(p.mu + row) : 0.f;
+    bool in_range = true;
     for (int ch = 0; ch < NCH; ++ch) {
       const int b = c.cnt & 1;
       const uint32_t abuf = c.buf + b * kSetB;
@@ -320,13 +355,7 @@ struct EpiRowScaleSwiGLU {
       }
       st_shared_v4(abuf + swz<32>(c.lane, 0), ap[0], ap[1], ap[2], ap[3]);
       st_shared_v4(abuf + swz<32>(c.lane, 1), ap[4], ap[5], ap[6], ap[7]);
-      if (p.save_y) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          st_shared_v4(ybuf + swz<128>(c.lane, k), __float_as_uint(v[4 * k]),
-                       __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
-                       __float_as_uint(v[4 * k + 3]));
-      }
+      if (p.save_y) in_range &= stage_f16x32(ybuf, c.lane, v);
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
@@ -336,6 +365,8 @@ struct EpiRowScaleSwiGLU {
       }
       ++c.cnt;
     }
+    // rows past M hold zeros and are never out of range
+    if (!__all_sync(0xffffffffu, in_range) && c.lane == 0) flag_error(c.e, kErrRange, 30);
     return true;
   }
 };
@@ -346,11 +377,11 @@ struct EpiRowScaleSwiGLU {
 //   v = r[m] * acc ; for columns < n_rope, inside each head_dim-wide head,
 //   (v_2i, v_2i+1) -> (v_2i c - v_2i+1 s, v_2i s + v_2i+1 c),
 //   (c, s) = cos_sin[pos(m), i], pos(m) = m mod seq_len
-// Output bf16; optionally also an fp32 copy kept for the backward's
-// relocated RMSNorm statistic.
+// Output bf16; optionally also an fp16 copy kept for the backward's
+// relocated RMSNorm statistic (range errors as in the SwiGLU epilogue).
 struct EpiRope {
   static constexpr int kBufB = 2048;   // 32 rows x 32 bf16
-  static constexpr int kSBufB = 4096;  // 32 rows x 32 fp32
+  static constexpr int kSBufB = 2048;  // 32 rows x 32 fp16
   static constexpr int kSetB = kBufB + kSBufB;
   static constexpr int kSmemPerWarp = 2 * kSetB;
   struct Params {
@@ -369,6 +400,7 @@ struct EpiRope {
     const float rr = (p.r == nullptr) ? 1.f : (row < g.M ? __ldg(p.r + row) : 0.f);
     const int pos = row < g.M ? row % p.seq_len : 0;
     const float4* csrow = reinterpret_cast<const float4*>(p.cs + (size_t)pos * (p.head_dim / 2));
+    bool in_range = true;
     for (int ch = 0; ch < NCH; ++ch) {
       const int b = c.cnt & 1;
       const uint32_t buf = c.buf + b * kSetB;
@@ -392,13 +424,7 @@ struct EpiRope {
         }
       }
       stage_bf16x32(buf, c.lane, v);
-      if (p.save) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          st_shared_v4(sbuf + swz<128>(c.lane, k), __float_as_uint(v[4 * k]),
-                       __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
-                       __float_as_uint(v[4 * k + 3]));
-      }
+      if (p.save) in_range &= stage_f16x32(sbuf, c.lane, v);
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
@@ -408,6 +434,7 @@ struct EpiRope {
       }
       ++c.cnt;
     }
+    if (!__all_sync(0xffffffffu, in_range) && c.lane == 0) flag_error(c.e, kErrRange, 31);
     return true;
   }
 };
@@ -538,7 +565,7 @@ struct EpiCEGrad {
 // LayerNorm statistics: spart_w = sum dy w1, spart_b = sum dy b1.
 template <bool LN>
 struct EpiSwiGLUBwd {
-  static constexpr int kYBufB = 4096;   // 32 rows x 32 fp32
+  static constexpr int kYBufB = 2048;   // 32 rows x 32 fp16
   static constexpr int kOBufB = 2048;   // 32 rows x 32 bf16
   static constexpr int kNL = 3;
   static constexpr int kSmemPerWarp = kNL * kYBufB + 2 * kOBufB;
@@ -584,12 +611,11 @@ struct EpiSwiGLUBwd {
       if (!c.wait(slot, 12)) return false;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {  // output chunk k = pairs 4k .. 4k+3
-        const uint4 y0 = ld_shared_v4(ybuf + swz<128>(c.lane, 2 * k));
-        const uint4 y1 = ld_shared_v4(ybuf + swz<128>(c.lane, 2 * k + 1));
-        const float gy[4] = {__uint_as_float(y0.x), __uint_as_float(y0.z), __uint_as_float(y1.x),
-                             __uint_as_float(y1.z)};
-        const float uy[4] = {__uint_as_float(y0.y), __uint_as_float(y0.w), __uint_as_float(y1.y),
-                             __uint_as_float(y1.w)};
+        const uint4 yv = ld_shared_v4(ybuf + swz<64>(c.lane, k));  // pairs 4k .. 4k+3
+        const float2 p0 = unpack_f16(yv.x), p1 = unpack_f16(yv.y), p2 = unpack_f16(yv.z),
+                     p3 = unpack_f16(yv.w);
+        const float gy[4] = {p0.x, p1.x, p2.x, p3.x};
+        const float uy[4] = {p0.y, p1.y, p2.y, p3.y};
         uint32_t outw[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {

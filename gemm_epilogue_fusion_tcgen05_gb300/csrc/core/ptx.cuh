@@ -6,12 +6,13 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace coda {
 
 // ----------------------------------------------------------------- error word
 // Codes shared with the host API (see include/coda.h).
-enum : int { kErrNone = 0, kErrTimeout = 4, kErrInvalid = 1 };
+enum : int { kErrNone = 0, kErrTimeout = 4, kErrInvalid = 1, kErrRange = 5 };
 
 struct DevError {
   int* word;                 // global error word (first error wins)
@@ -28,6 +29,12 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 __device__ __forceinline__ void record_error(const DevError& e, int code, int where) {
   if (e.word) atomicCAS(e.word, 0, (code & 0xff) | (where << 8));
   if (e.abort_flag) *e.abort_flag = 1;
+}
+
+// Record an error without asking the other roles to stop: the kernel runs
+// to completion and the host learns of it from the error word.
+__device__ __forceinline__ void flag_error(const DevError& e, int code, int where) {
+  if (e.word) atomicCAS(e.word, 0, (code & 0xff) | (where << 8));
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

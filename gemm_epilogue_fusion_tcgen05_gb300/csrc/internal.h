@@ -123,7 +123,7 @@ cudaError_t launch_col_reduce(const float* part, int nparts, int N, float* out, 
 cudaError_t launch_ce_combine(const float2* part, int nparts, const float* tlogit, const int* targets,
                               int M, int V, float* lse, float* loss, int* err, cudaStream_t st);
 cudaError_t launch_rope_table(float2* cs, int seq_len, int head_dim, double theta, cudaStream_t st);
-cudaError_t launch_rope_bwd(const bf16* d, const float* q, const float* r, const float2* cs,
+cudaError_t launch_rope_bwd(const bf16* d, const __half* q, const float* r, const float2* cs,
                             int seq_len, int head_dim, int n_rope, bf16* out, float* s, int M, int N,
                             float inv_d, cudaStream_t st);
 cudaError_t launch_ln_stats(const float* part_sq, const float* part_sum, int nparts, int M, float inv_d,

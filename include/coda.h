@@ -33,8 +33,10 @@
  *       CODA_ERR_LAUNCH         a CUDA error at launch (text from
  *                               coda_last_error_string()).
  *     Device-side failures (a bounded wait that ran out, an out-of-range CE
- *     target) are recorded in a device error word and reported by
- *     coda_get_device_error().
+ *     target, a value beyond the fp16 range in a saved fp16 copy) are
+ *     recorded in a device error word and reported by
+ *     coda_get_device_error() (CODA_ERR_TIMEOUT, CODA_ERR_INVALID_VALUE,
+ *     CODA_ERR_RANGE).
  *   - Partial buffers: the GEMM epilogues write tile-local partials that a
  *     small auxiliary kernel reduces ([pith] Fig. 4 caption). Their shapes
  *     use coda_col_tiles(N) = ceil(N / 256) (one partial per 256-column
@@ -55,7 +57,8 @@ typedef enum {
   CODA_ERR_INVALID_VALUE = 1,
   CODA_ERR_UNSUPPORTED = 2,
   CODA_ERR_LAUNCH = 3,
-  CODA_ERR_TIMEOUT = 4
+  CODA_ERR_TIMEOUT = 4,
+  CODA_ERR_RANGE = 5
 } coda_status_t;
 
 /* Opaque CUDA stream (identical to cudaStream_t). */
@@ -123,10 +126,13 @@ coda_status_t coda_row_rms(const float* part, int nparts, int M, int d, float ep
  * y = r (h2 W1); [pith] Fig. 7: SwiGLU combines gate and value streams):
  *   y = r[m] * (hg W1)   (columns 2k = gate g_k, 2k+1 = up u_k)
  *   a[m, k] = silu(g_k) * u_k          (bf16 [M, two_f / 2])
- *   y_save (nullable): fp32 [M, two_f], the scaled y kept for the backward
- *   (fp32 because the relocated RMSNorm statistic of the backward sums 2f
- *   products of y with heavy cancellation; bf16 storage of y alone would
- *   move it by ~5e-3 relative).
+ *   y_save (nullable): fp16 [M, two_f], the scaled y kept for the backward.
+ *   Not bf16: the relocated RMSNorm statistic of the backward sums 2f
+ *   products of y with heavy cancellation, and bf16 storage of y alone moves
+ *   it by ~1e-3..5e-3 relative; fp16 (11-bit significand) keeps it near
+ *   1e-4 at half the bytes of fp32. A y of magnitude >= 65520 (or NaN) is
+ *   stored as inf/NaN and raises CODA_ERR_RANGE in coda_get_device_error();
+ *   a and the other outputs are still written.
  * hg bf16 [M, K]; W1 bf16 [K, two_f]; r fp32 [M]; two_f even. */
 coda_status_t coda_gemm_rowscale_swiglu(const void* hg, const void* W1, const float* r, void* a,
                                         void* y_save, int M, int two_f, int K,
@@ -138,13 +144,14 @@ coda_status_t coda_gemm_rowscale_swiglu(const void* hg, const void* W1, const fl
  *   for n < n_rope_cols, inside each head_dim-wide head, pair (2i, 2i+1):
  *     v'_2i = v_2i c - v_2i+1 s,  v'_2i+1 = v_2i s + v_2i+1 c,
  *     (c, s) = cos_sin[m mod seq_len, i]
- *   out bf16 [M, N]; out_f32 (nullable) fp32 [M, N], the same values kept
- *   unrounded for the backward's relocated RMSNorm statistic
- *   (coda_gemm_rope_bwd). A bf16 [M, K]; W bf16 [K, N];
+ *   out bf16 [M, N]; out_f16 (nullable) fp16 [M, N], the same values kept
+ *   with a longer significand for the backward's relocated RMSNorm statistic
+ *   (coda_gemm_rope_bwd); range errors as for y_save of
+ *   coda_gemm_rowscale_swiglu. A bf16 [M, K]; W bf16 [K, N];
  *   cos_sin fp32 [seq_len, head_dim/2, 2] (see coda_rope_table).
  *   head_dim % 32 == 0, n_rope_cols % head_dim == 0, n_rope_cols <= N. */
 coda_status_t coda_gemm_rope(const void* A, const void* W, const float* r, const float* cos_sin,
-                             int seq_len, int head_dim, int n_rope_cols, void* out, float* out_f32,
+                             int seq_len, int head_dim, int n_rope_cols, void* out, void* out_f16,
                              int M, int N, int K, coda_stream_t stream);
 
 /* Fills cos_sin[p, i] = (cos(p t_i), sin(p t_i)), t_i = theta^(-2i/head_dim),
@@ -226,7 +233,7 @@ coda_status_t coda_lmhead_ce_bwd(const void* hidden, const void* W, const int32_
  *   dg = da u sg (1 + g (1 - sg)) ; du = da g sg
  *   dyhat[m, 2k..2k+1] = r[m] (dg, du)            (bf16 [M, 2f])
  *   spart[t, m] = sum over tile t of dg g + du u  (fp32 [coda_col_tiles(f), M])
- * dout bf16 [M, d]; W2 bf16 [f, d]; y fp32 [M, 2f] (as saved by
+ * dout bf16 [M, d]; W2 bf16 [f, d]; y fp16 [M, 2f] (as saved by
  * coda_gemm_rowscale_swiglu); r fp32 [M]. */
 coda_status_t coda_gemm_rowscale_swiglu_bwd(const void* dout, const void* W2, const void* y,
                                             const float* r, void* dyhat, float* spart, int M,
@@ -257,10 +264,10 @@ coda_status_t coda_col_reduce(const float* part, int nparts, int N, float* out,
  * its own bandwidth-bound kernel:
  *   dqkv_hat = r[m] R(pos)^T dqkv_rot           (bf16 [M, N])
  *   s[m] = (1/d) sum_n dqkv_rot[m, n] qkv_rot[m, n]   (fp32 [M])
- * dqkv_rot bf16 [M, N]; qkv_rot fp32 [M, N] (the out_f32 copy saved by
+ * dqkv_rot bf16 [M, N]; qkv_rot fp16 [M, N] (the out_f16 copy saved by
  * coda_gemm_rope); r fp32 [M] (nullable: no scale); cos_sin as in
  * coda_gemm_rope; d = width of the normalised input of the QKV GEMM. */
-coda_status_t coda_gemm_rope_bwd(const void* dqkv_rot, const float* qkv_rot, const float* r,
+coda_status_t coda_gemm_rope_bwd(const void* dqkv_rot, const void* qkv_rot, const float* r,
                                  const float* cos_sin, int seq_len, int head_dim, int n_rope_cols,
                                  void* dqkv_hat, float* s, int M, int N, int d,
                                  coda_stream_t stream);
@@ -288,15 +295,16 @@ coda_status_t coda_row_ln(const float* part_sq, const float* part_sum, int npart
                           float eps, float* r, float* mu, coda_stream_t stream);
 
 /* GEMM 2: y = r[m] (hg W1) - (r mu)[m] w1[n] + b1[n]; a = SwiGLU(y) (bf16
- * [M, two_f/2]); y_save (nullable) fp32 [M, two_f]. */
+ * [M, two_f/2]); y_save (nullable) fp16 [M, two_f] (as for
+ * coda_gemm_rowscale_swiglu). */
 coda_status_t coda_gemm_ln_rowscale_swiglu(const void* hg, const void* W1, const float* r,
                                            const float* mu, const float* w1, const float* b1,
-                                           void* a, float* y_save, int M, int two_f, int K,
+                                           void* a, void* y_save, int M, int two_f, int K,
                                            coda_stream_t stream);
 
 /* SwiGLU backward as coda_gemm_rowscale_swiglu_bwd, plus the row partials
  * spart_w = sum dy w1 and spart_b = sum dy b1 (fp32 [coda_col_tiles(f), M]). */
-coda_status_t coda_gemm_ln_rowscale_swiglu_bwd(const void* dout, const void* W2, const float* y,
+coda_status_t coda_gemm_ln_rowscale_swiglu_bwd(const void* dout, const void* W2, const void* y,
                                                const float* r, const float* w1, const float* b1,
                                                void* dyhat, float* spart, float* spart_w,
                                                float* spart_b, int M, int f, int d,

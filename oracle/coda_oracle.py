@@ -70,8 +70,23 @@ def bf16_round(a) -> np.ndarray:
     return r
 
 
+def f16_round(a) -> np.ndarray:
+    """Round fp64 values to the nearest IEEE binary16 value (ties to even),
+    returned as fp64: numpy's float16 conversion, which rounds correctly
+    from fp64. 11 significant bits; magnitudes from 65520 up become inf."""
+    with np.errstate(over="ignore"):
+        return np.asarray(a, dtype=f64).astype(np.float16).astype(f64)
+
+
 def _store(store_bf16: bool):
     return bf16_round if store_bf16 else (lambda t: t)
+
+
+def _store_saved(store_bf16: bool):
+    """The storage point of the copies the rewritten forward keeps only for
+    the backward's relocated statistics (y, qkv_save): fp16, whose 11-bit
+    significand keeps those statistics within 1e-3 where bf16 would not."""
+    return f16_round if store_bf16 else (lambda t: t)
 
 
 # --------------------------------------------------------------------------
@@ -144,14 +159,14 @@ def mlp_fwd_reparam(x, z, W0, W1, W2, gamma, eps: float = EPS,
                          weight multiplies it)
         auxiliary:       r = 1/sqrt(mean(h^2) + eps)
         GEMM 2 epilogue: y = r * (hg W1)  (delayed row scale, saved for the
-                         backward in fp32), a = silu(y_gate) * y_up (stored)
+                         backward in fp16), a = silu(y_gate) * y_up (stored)
         GEMM 3:          out = a W2
     With store_bf16, each tensor the rewritten kernels store in bf16 (h, hg,
     a, out) is rounded to bf16 where it is written; its consumers read the
     rounded value, the statistics are taken before rounding. The saved y is
-    kept at full precision (its fp32 storage error is far below every
-    tolerance)."""
+    rounded to fp16 (a is computed from the unrounded y)."""
     st = _store(store_bf16)
+    sv = _store_saved(store_bf16)
     x, z, W0, W1, W2, gamma = (np.asarray(t, dtype=f64) for t in (x, z, W0, W1, W2, gamma))
     h_acc = x @ W0 + z
     r = rms_factor(h_acc, eps)
@@ -159,7 +174,7 @@ def mlp_fwd_reparam(x, z, W0, W1, W2, gamma, eps: float = EPS,
     hg = st(h_acc * gamma[None, :])
     y_acc = r[:, None] * (hg @ W1)
     a = st(swiglu(y_acc))
-    y = y_acc
+    y = sv(y_acc)
     out = st(a @ W2)
     return {"h": h, "r": r, "hg": hg, "y": y, "a": a, "out": out}
 
@@ -292,8 +307,10 @@ def ln_mlp_fwd_reparam(x, z, W0, W1, W2, gamma, beta, eps: float = EPS,
     hg = h * gamma and emits per-row sums of h and h^2; the auxiliary step
     gives mu and r; with the n-vectors w1 = gamma W1 and b1 = beta W1,
         y = r (hg W1) - (r mu) w1 + b1
-    which equals (r (h - mu) gamma + beta) W1."""
+    which equals (r (h - mu) gamma + beta) W1. With store_bf16 the storage
+    points are those of the RMSNorm form (y saved in fp16)."""
     st = _store(store_bf16)
+    sv = _store_saved(store_bf16)
     x, z, W0, W1, W2, gamma, beta = (np.asarray(t, dtype=f64) for t in (x, z, W0, W1, W2, gamma, beta))
     h_acc = x @ W0 + z
     d = h_acc.shape[1]
@@ -308,7 +325,8 @@ def ln_mlp_fwd_reparam(x, z, W0, W1, W2, gamma, beta, eps: float = EPS,
     y = r[:, None] * (hg @ W1) - (r * mu)[:, None] * w1[None, :] + b1[None, :]
     a = st(swiglu(y))
     out = st(a @ W2)
-    return {"h": h, "hg": hg, "mu": mu, "r": r, "w1": w1, "b1": b1, "y": y, "a": a, "out": out}
+    return {"h": h, "hg": hg, "mu": mu, "r": r, "w1": w1, "b1": b1, "y": sv(y), "a": a,
+            "out": out}
 
 
 def ln_mlp_bwd_reparam(fwd, x, W0, W1, W2, gamma, beta, dout,
@@ -550,8 +568,10 @@ def block8b_fwd_reparam(o, z, Wo, W1, W2, gamma2, gamma1, Wqkv, pos, n_rope_cols
     With store_bf16, the tensors the rewritten kernels store in bf16 (h, hg,
     a, out, outg, qkv) are rounded where they are written and read back
     rounded; y and the copy of qkv kept for the backward's statistic
-    (``qkv_save``) stay at full precision (saved in fp32)."""
+    (``qkv_save``) are rounded to fp16 (the bf16 outputs come from the
+    unrounded values)."""
     st = _store(store_bf16)
+    sv = _store_saved(store_bf16)
     o, z, Wo, W1, W2, gamma2, gamma1, Wqkv = (np.asarray(t, dtype=f64) for t in
                                                (o, z, Wo, W1, W2, gamma2, gamma1, Wqkv))
     h_acc = o @ Wo + z
@@ -565,8 +585,8 @@ def block8b_fwd_reparam(o, z, Wo, W1, W2, gamma2, gamma1, Wqkv, pos, n_rope_cols
     out = st(out_acc)
     outg = st(out_acc * gamma1[None, :])
     qkv_acc = rope_apply(r1[:, None] * (outg @ Wqkv), pos, n_rope_cols, head_dim, theta)
-    return {"h": h, "hg": hg, "r": r, "y": y, "a": a, "out": out, "outg": outg, "r1": r1,
-            "qkv": st(qkv_acc), "qkv_save": qkv_acc}
+    return {"h": h, "hg": hg, "r": r, "y": sv(y), "a": a, "out": out, "outg": outg, "r1": r1,
+            "qkv": st(qkv_acc), "qkv_save": sv(qkv_acc)}
 
 
 def block8b_bwd_reparam(fwd, o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres, pos,

@@ -139,6 +139,29 @@ def test_block8b_small(coda):
     assert_close("s (storage-rounded oracle)", bw["s"], br["s"], TOL_F32)
 
 
+def test_saved_fp16_copy_out_of_range_reports_error(coda):
+    """A y beyond the fp16 range cannot be saved for the backward: the kernel
+    finishes, a is still written, and the host gets CODA_ERR_RANGE once."""
+    M, K, two_f = 128, 64, 512
+    g = torch.Generator().manual_seed(5)
+    hg = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    W1 = torch.randn(K, two_f, generator=g).to(torch.bfloat16).cuda()
+    r = torch.ones(M, dtype=torch.float32, device="cuda")
+    r[7] = 1e6  # row 7: |y| ~ 1e7
+    a = torch.empty(M, two_f // 2, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(M, two_f, dtype=torch.float16, device="cuda")
+    coda.coda_gemm_rowscale_swiglu(hg, W1, r, a, y)
+    assert coda.get_device_error() == coda.CODA_ERR_RANGE
+    assert coda.get_device_error() == 0  # reading the word clears it
+    assert torch.isinf(y[7].float()).any() and torch.isfinite(y[:7].float()).all()
+    ref = (hg.double() @ W1.double()) * r.double()[:, None]
+    a_ref = torch.nn.functional.silu(ref[:, 0::2]) * ref[:, 1::2]
+    assert_close("a (rows in range)", a[:7], a_ref[:7].cpu().numpy(), TOL_BF16)
+    # the same call without the saved copy has nothing to report
+    coda.coda_gemm_rowscale_swiglu(hg, W1, r, a, None)
+    assert coda.get_device_error() == 0
+
+
 def test_rope_table(coda):
     from gemm_epilogue_fusion_tcgen05_gb300 import blocks
     cs = blocks.rope_table(4096, 128, 500000.0, "cuda").cpu().double().numpy()

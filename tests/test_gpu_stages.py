@@ -47,7 +47,7 @@ def _t(a, dtype):
 def test_swiglu_bwd_stage_full_size(coda, oracle_1b):
     sh, inp, st, sb = oracle_1b
     M, d, f = sh.M, sh.d, sh.f
-    y = _t(st["y"], torch.float32)
+    y = _t(st["y"], torch.float16)
     r = _t(st["r"], torch.float32)
     dyhat = torch.empty((M, 2 * f), dtype=torch.bfloat16, device="cuda")
     spart = torch.empty((coda.col_tiles(f), M), dtype=torch.float32, device="cuda")
@@ -107,7 +107,7 @@ def test_rope_bwd_stage_8b_shape(coda):
     cs = blocks.rope_table(sh.seq_len, sh.head_dim, sh.theta, "cuda")
     out = torch.empty((L, N), dtype=torch.bfloat16, device="cuda")
     s1 = torch.empty((L,), dtype=torch.float32, device="cuda")
-    coda.coda_gemm_rope_bwd(_t(dq, torch.bfloat16), _t(q, torch.float32), _t(r1, torch.float32), cs,
+    coda.coda_gemm_rope_bwd(_t(dq, torch.bfloat16), _t(q, torch.float16), _t(r1, torch.float32), cs,
                             sh.seq_len, sh.head_dim, sh.n_rope_cols, out, s1, sh.d)
     torch.cuda.synchronize()
     assert coda.get_device_error() == 0

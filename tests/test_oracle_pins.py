@@ -43,6 +43,33 @@ def test_bf16_round_matches_torch_on_fp32_values():
     assert np.array_equal(got, ref)
 
 
+def test_f16_round_matches_torch_and_ieee_binary16():
+    # torch's float32 -> float16 conversion is IEEE round-to-nearest-even
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 12, 200000))).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float16).to(torch.float64).numpy()
+    assert np.array_equal(O.f16_round(v.astype(np.float64)), ref)
+    ulp = 2.0 ** -10                                          # spacing of binary16 at 1
+    assert O.f16_round(1 + ulp / 2) == 1.0                    # tie -> even (down)
+    assert O.f16_round(1 + 3 * ulp / 2) == 1 + 2 * ulp        # tie -> even (up)
+    assert O.f16_round(1 + ulp / 2 + 2 ** -30) == 1 + ulp
+    assert O.f16_round(65504.0) == 65504.0                    # largest finite
+    assert O.f16_round(65519.99) == 65504.0
+    assert np.isinf(O.f16_round(65520.0))                     # rounds past the top
+    assert O.f16_round(2.0 ** -24) == 2.0 ** -24              # smallest subnormal
+    assert O.f16_round(2.0 ** -26) == 0.0
+
+
+def test_saved_copies_are_fp16_rounded_in_the_storage_form():
+    inp = rand_block(M=4, d=16, f=8, seed=9)
+    fr = O.mlp_fwd_reparam(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"],
+                           store_bf16=True)
+    fe = O.mlp_fwd_reparam(inp["x"], inp["z"], inp["W0"], inp["W1"], inp["W2"], inp["gamma"])
+    assert np.array_equal(fr["y"], O.f16_round(fr["y"]))
+    assert not np.array_equal(fe["y"], O.f16_round(fe["y"]))
+    assert rel(fr["y"], fe["y"]) < 2.0 ** -11 * 1.01 + 1e-2  # hg's bf16 rounding dominates
+
+
 def test_bf16_round_ties_to_even_and_nearest():
     one = 1.0
     ulp = 2.0 ** -7
