@@ -290,11 +290,49 @@ class Step:
 
     # per-step inputs and results for the end-to-end measurement
     def host_io(self):
-        ins = [self.i1["x"], self.i1["z"], self.i1["dout"], self.i2["hidden"], self.i2["targets"]]
-        if self.with_8b:
-            ins += [self.i4["o"], self.i4["z"], self.i4["dqkv"], self.i4["dres"]]
+        ins = [t for group, _ in self.input_groups() for t in group]
         outs = [self.o2["loss"], self.o2["lse"], self.b1["dgamma"]]
         return ins, outs
+
+    def input_groups(self):
+        """The step's per-step inputs in the order the step first reads them,
+        each group with the first call that reads any of its tensors."""
+        groups = [([self.i1["x"], self.i1["z"]], "1b.gemm_resid_norm_stats"),
+                  ([self.i2["hidden"], self.i2["targets"]], "lmhead_ce"),
+                  ([self.i1["dout"]], "1b.gemm_rowscale_swiglu_bwd")]
+        if self.with_8b:
+            groups += [([self.i4["o"], self.i4["z"]], "8b.gemm_resid_norm_stats(Wo)"),
+                       ([self.i4["dqkv"], self.i4["dres"]], "8b.rope_bwd")]
+        return groups
+
+    def run_from_host(self, h_groups, h_outs, copy_stream):
+        """One end-to-end step: each input group is copied host -> device on
+        `copy_stream` (after everything already queued on the compute
+        stream), and the compute stream waits for a group only right before
+        the first call that reads it, so the copies of later groups overlap
+        the kernels of earlier ones. The results are read back at the end."""
+        main = torch.cuda.current_stream()
+        copy_stream.wait_stream(main)
+        first = {}
+        for gi, (group, name) in enumerate(self.input_groups()):
+            ev = torch.cuda.Event()
+            with torch.cuda.stream(copy_stream):
+                for hsrc, ddst in zip(h_groups[gi], group):
+                    ddst.copy_(hsrc, non_blocking=True)
+                ev.record(copy_stream)
+            first.setdefault(name, []).append(ev)
+        pending = [ev for evs in first.values() for ev in evs]
+        for name, fl, fn, nl in self.calls:
+            for ev in first.pop(name, []):
+                main.wait_event(ev)
+            fn()
+        for evs in first.values():  # groups whose reader is not in this step
+            for ev in evs:
+                main.wait_event(ev)
+        outs = self.host_io()[1]
+        for dsrc, hdst in zip(outs, h_outs):
+            hdst.copy_(dsrc, non_blocking=True)
+        return pending
 
 
 def run_coda(args):
@@ -362,22 +400,19 @@ def run_coda(args):
     # end-to-end through the public API with host buffers: copy this step's
     # inputs host -> device from pinned memory, run, read the results back
     ins, outs = step.host_io()
-    h_ins = [t.cpu().pin_memory() for t in ins]
+    h_groups = [[t.cpu().pin_memory() for t in group] for group, _ in step.input_groups()]
     h_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    h2d = sum(t.numel() * t.element_size() for t in h_ins)
+    h2d = sum(t.numel() * t.element_size() for g in h_groups for t in g)
     d2h = sum(t.numel() * t.element_size() for t in h_outs)
     e2e_steps = 0 if args.only else max(2, min(args.steps, 5))
+    copy_stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
     for i in range(e2e_steps):
         flush.fill_(float(i))
         e0.record(stream)
-        for hsrc, ddst in zip(h_ins, ins):
-            ddst.copy_(hsrc, non_blocking=True)
-        step.run()
-        for dsrc, hdst in zip(outs, h_outs):
-            hdst.copy_(dsrc, non_blocking=True)
+        step.run_from_host(h_groups, h_outs, copy_stream)
         e1.record(stream)
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
@@ -425,13 +460,15 @@ def run_coda(args):
                      "traffic": traffic},
         "e2e": {"value": round(e2e_value, 2) if e2e_value else None, "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "per input group on a copy stream; compute waits for a group "
+                          "only before its first reader"},
         "clocks": clk,
         "parts_ms": {step.calls[k][0]: round(per_call[k], 4) for k in range(n)},
     }
     if args.only:
         line["config"]["only"] = args.only
-    if not args.only:
+    if not args.only and not args.no_next_rows:
         line["next_rows"] = next_rows(step, flush)
     if not args.only and not args.no_unfused:
         ref_ms = unfused_reference(step, flush)
@@ -759,6 +796,8 @@ def main():
     ap.add_argument("--no-8b", action="store_true", help="leave the 8B-shaped block out of the step")
     ap.add_argument("--primitives", action="store_true",
                     help="epilogue-primitive microbenchmarks instead of the step")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the rows timed beyond the step (CE backward, LayerNorm block)")
     ap.add_argument("--no-unfused", action="store_true",
                     help="skip the unfused PyTorch reference sequence")
     ap.add_argument("--only", default="", help="time only these calls (comma-separated names; "
