@@ -16,19 +16,31 @@
 //   tempty[b] (even CTA)  8 arrivals (4 epilogue warps x 2 CTAs)
 //   drain     (both)      last MMA commit: nothing reads shared memory or
 //                          TMEM any more, so both CTAs may leave
+//
+// Two-slab form (MS = 2): each CTA holds 2 x 128 rows of A and the pair
+// computes a 512 x BN tile with two MMAs per K step that share the B half, so
+// every byte of B staged in shared memory feeds twice the tensor-core work
+// and the operand bytes per FLOP drop by a quarter; the same bytes in flight
+// then cover a third more MMA time. Both slabs' accumulators fill TMEM, so
+// there is one accumulator buffer and the epilogue does not overlap the next
+// tile's MMA: the form pays off for long K, where the epilogue is rare.
 #pragma once
 #include "gemm.cuh"
 
 namespace coda {
 
-template <int BN_, bool A_MN_, bool B_MN_, class Epi_>
+template <int BN_, bool A_MN_, bool B_MN_, class Epi_, int MS_ = 1>
 struct Gemm2Traits {
   static constexpr int BN = BN_;
   static constexpr bool A_MN = A_MN_;
   static constexpr bool B_MN = B_MN_;
   using Epi = Epi_;
+  static constexpr int MS = MS_;                          // 128-row slabs of A per CTA
+  static constexpr int NACC = MS == 1 ? 2 : 1;            // accumulator buffers in TMEM
+  static_assert(MS == 1 || MS == 2, "MS");
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int A_BYTES = kBM * kBK * 2;          // this CTA's 128 rows
+  static constexpr int SLAB_BYTES = kBM * kBK * 2;        // one 128-row slab of A
+  static constexpr int A_BYTES = MS * SLAB_BYTES;         // this CTA's 128 * MS rows
   static constexpr int B_BYTES = (BN / 2) * kBK * 2;     // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_BYTES = Epi::kSmemPerWarp * kEpiWarps;
@@ -38,7 +50,7 @@ struct Gemm2Traits {
   static_assert(STAGES >= 3, "not enough shared memory for three pipeline stages");
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= kSmemMax, "shared memory budget");
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int TMEM_COLS = NACC * MS * BN;
   static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns must be a power of two");
   static_assert(BN % 128 == 0 && BN <= 256, "BN");
   static constexpr uint32_t IDESC = idesc_bf16_f32(2 * kBM, BN, A_MN, B_MN);
@@ -114,7 +126,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
       for (int t = pair; t < g.num_tiles && ok; t += npairs) {
         int mb, nb;
         tile_coords(g, t, mb, nb);
-        const int m0 = mb * 2 * kBM + (int)rank * kBM;
+        const int m0 = (mb * 2 + (int)rank) * T::MS * kBM;
         const int n0 = nb * BN + (int)rank * (BN / 2);
         for (int kb = 0; kb < g.num_kb; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, e, 21)) {
@@ -128,14 +140,19 @@ __global__ void __launch_bounds__(T::kThreads, 1)
           const int k0 = kb * kBK;
           // the band's stationary operand stays in L2 (evict_last); the
           // other streams past with the default policy
-          if constexpr (!T::A_MN) {
-            if (g.along_m) tma_load_2d_pair_hint(&tmA, a_dst, fb, k0, m0, pol_keep);
-            else tma_load_2d_pair(&tmA, a_dst, fb, k0, m0);
-          } else {
 #pragma unroll
-            for (int j = 0; j < kBM / 64; ++j) {
-              if (g.along_m) tma_load_2d_pair_hint(&tmA, a_dst + j * 8192, fb, m0 + j * 64, k0, pol_keep);
-              else tma_load_2d_pair(&tmA, a_dst + j * 8192, fb, m0 + j * 64, k0);
+          for (int i = 0; i < T::MS; ++i) {
+            const uint32_t ad = a_dst + i * T::SLAB_BYTES;
+            const int mi = m0 + i * kBM;
+            if constexpr (!T::A_MN) {
+              if (g.along_m) tma_load_2d_pair_hint(&tmA, ad, fb, k0, mi, pol_keep);
+              else tma_load_2d_pair(&tmA, ad, fb, k0, mi);
+            } else {
+#pragma unroll
+              for (int j = 0; j < kBM / 64; ++j) {
+                if (g.along_m) tma_load_2d_pair_hint(&tmA, ad + j * 8192, fb, mi + j * 64, k0, pol_keep);
+                else tma_load_2d_pair(&tmA, ad + j * 8192, fb, mi + j * 64, k0);
+              }
             }
           }
           if constexpr (!T::B_MN) {
@@ -170,13 +187,13 @@ __global__ void __launch_bounds__(T::kThreads, 1)
         uint32_t phase = 0;
         bool ok = true;
         for (int t = pair; t < g.num_tiles && ok; t += npairs, ++li) {
-          const int acc = li & 1;
-          if (!mbar_wait_cluster(tempty(acc), ((li >> 1) & 1) ^ 1u, e, 22)) {
+          const int acc = li % T::NACC;
+          if (!mbar_wait_cluster(tempty(acc), ((li / T::NACC) & 1) ^ 1u, e, 22)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + acc * BN;
+          const uint32_t d_tmem = tmem_base + acc * T::MS * BN;
           for (int kb = 0; kb < g.num_kb; ++kb) {
             if (!mbar_wait_cluster(full(stage), phase, e, 23)) {
               ok = false;
@@ -187,11 +204,15 @@ __global__ void __launch_bounds__(T::kThreads, 1)
             const uint32_t b_s = sB + stage * T::B_BYTES;
 #pragma unroll
             for (int k = 0; k < kBK / kUK; ++k) {
-              const uint64_t ad = T::A_MN ? smem_desc_sw128(a_s + k * 2048, 8192, 1024)
-                                          : smem_desc_sw128(a_s + k * 32, 16, 1024);
               const uint64_t bd = T::B_MN ? smem_desc_sw128(b_s + k * 2048, 8192, 1024)
                                           : smem_desc_sw128(b_s + k * 32, 16, 1024);
-              mma_bf16_pair(d_tmem, ad, bd, T::IDESC, (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+              for (int i = 0; i < T::MS; ++i) {
+                const uint32_t as = a_s + i * T::SLAB_BYTES;
+                const uint64_t ad = T::A_MN ? smem_desc_sw128(as + k * 2048, 8192, 1024)
+                                            : smem_desc_sw128(as + k * 32, 16, 1024);
+                mma_bf16_pair(d_tmem + i * BN, ad, bd, T::IDESC, (kb | k) != 0 ? 1u : 0u);
+              }
             }
             mma_commit_pair(empty(stage), 0x3);
             if (++stage == S) {
@@ -226,15 +247,21 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     for (int t = pair; t < g.num_tiles; t += npairs, ++li) {
       int mb, nb;
       tile_coords(g, t, mb, nb);
-      const int m0 = mb * 2 * kBM + (int)rank * kBM, n0 = nb * BN;
-      const int acc = li & 1;
-      T::Epi::template prefetch<BN>(ep, ctx, g, m0, n0);
-      bool ok = mbar_wait_cluster(tfull(acc), (li >> 1) & 1, e, 24);
+      const int m_cta = (mb * 2 + (int)rank) * T::MS * kBM, n0 = nb * BN;
+      const int acc = li % T::NACC;
+      T::Epi::template prefetch<BN>(ep, ctx, g, m_cta, n0);
+      bool ok = mbar_wait_cluster(tfull(acc), (li / T::NACC) & 1, e, 24);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(32 * ctx.q) << 16) + acc * BN;
-      ok = T::Epi::template tile<BN>(ep, ctx, g, m0, n0, nb, taddr);
+#pragma unroll 1
+      for (int i = 0; i < T::MS && ok; ++i) {
+        const int m0 = m_cta + i * kBM;
+        if (i > 0) T::Epi::template prefetch<BN>(ep, ctx, g, m0, n0);
+        const uint32_t taddr =
+            tmem_base + ((uint32_t)(32 * ctx.q) << 16) + (acc * T::MS + i) * BN;
+        ok = T::Epi::template tile<BN>(ep, ctx, g, m0, n0, nb, taddr);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty(acc), 0));

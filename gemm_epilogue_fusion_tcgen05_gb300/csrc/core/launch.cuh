@@ -48,6 +48,29 @@ inline void choose_tile_order(GemmArgs& g, int bm, int bn, int K, int conc) {
   }
 }
 
+// Whether the two-slab pair tile (512 x bn, see gemm2.cuh) should beat the
+// one-slab tile (256 x bn) on an M x N x K GEMM with `pairs` co-resident CTA
+// pairs. Two slabs move a quarter fewer operand bytes per FLOP (measured
+// 1.25x the throughput on weight-gradient shapes with K = 16384 at equal wave
+// counts), but they halve the tile count (coarser waves) and the epilogue no
+// longer overlaps the next tile's MMA (about `epi_kb` K-blocks of MMA time
+// per tile for a 256 x 256 fp32 output per CTA). Estimated time in units of
+// one 256-row tile's mainloop of K:
+//   one slab   ceil(T1 / P)
+//   two slabs  ceil(T2 / P) * (2 * kTwoSlabCost + epi_kb / kblocks)
+// Two slabs are taken only when the estimate is at least 3 % lower (at
+// K = 8192 with 7 one-slab waves against 4 two-slab waves they measured even).
+constexpr int kTwoSlabMinK = 8192;
+constexpr double kTwoSlabCost = 0.80;
+inline bool prefer_two_slabs(int M, int N, int K, int bn, int pairs, double epi_kb = 16.0) {
+  if (K < kTwoSlabMinK || pairs <= 0) return false;
+  const double tn = (double)((N + bn - 1) / bn);
+  const double t1 = (double)((M + 255) / 256) * tn, t2 = (double)((M + 511) / 512) * tn;
+  const double w1 = std::ceil(t1 / pairs), w2 = std::ceil(t2 / pairs);
+  const double kblocks = (double)((K + kBK - 1) / kBK);
+  return w2 * (2.0 * kTwoSlabCost + epi_kb / kblocks) < 0.97 * w1;
+}
+
 template <class T>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB,
                         const typename T::Epi::Params& ep, int M, int N, int K, const LaunchCtx& lc) {
@@ -115,12 +138,13 @@ cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
   g.M = M;
   g.N = N;
   g.K = K;
-  g.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
+  constexpr int kPairRows = 2 * T::MS * kBM;
+  g.tiles_m = (M + kPairRows - 1) / kPairRows;
   g.tiles_n = (N + T::BN - 1) / T::BN;
   g.num_tiles = g.tiles_m * g.tiles_n;
   g.num_kb = (K + kBK - 1) / kBK;
   const int pairs = g.num_tiles < pairs_max ? g.num_tiles : pairs_max;
-  choose_tile_order(g, 2 * kBM, T::BN, K, pairs);
+  choose_tile_order(g, kPairRows, T::BN, K, pairs);
   g.err = lc.err;
   g.timeout_ns = lc.timeout_ns;
   cfg.gridDim = dim3(2 * pairs, 1, 1);

@@ -4,10 +4,10 @@
 
 namespace coda {
 
-template <bool AMN, bool BMN, bool F32, bool R, bool Q>
+template <bool AMN, bool BMN, bool F32, bool R, bool Q, int MS = 1>
 static cudaError_t plain_impl(const PlainArgs& a, const LaunchCtx& lc) {
   using E = EpiPlain<F32, R, Q>;
-  using T = Gemm2Traits<kTileN, AMN, BMN, E>;
+  using T = Gemm2Traits<kTileN, AMN, BMN, E, MS>;
   typename E::Params p{};
   p.tm_c = a.tmC;
   p.tm_r = a.tmR;
@@ -19,12 +19,17 @@ cudaError_t launch_plain_other(const PlainArgs& a, const LaunchCtx& lc);
 
 cudaError_t launch_plain(const PlainArgs& a, const LaunchCtx& lc) {
   if (!a.a_mn && a.b_mn) {
-    if (a.out_f32) return a.resid ? plain_impl<false, true, true, true, false>(a, lc)
-                                  : plain_impl<false, true, true, false, false>(a, lc);
+    const bool two = prefer_two_slabs(a.M, a.N, a.K, kTileN, lc.num_sms / 2);
+    if (a.out_f32) {
+      if (a.resid) return plain_impl<false, true, true, true, false>(a, lc);
+      return two ? plain_impl<false, true, true, false, false, 2>(a, lc)
+                 : plain_impl<false, true, true, false, false>(a, lc);
+    }
     if (a.resid && a.rowsq) return plain_impl<false, true, false, true, true>(a, lc);
     if (a.resid) return plain_impl<false, true, false, true, false>(a, lc);
     if (a.rowsq) return plain_impl<false, true, false, false, true>(a, lc);
-    return plain_impl<false, true, false, false, false>(a, lc);
+    return two ? plain_impl<false, true, false, false, false, 2>(a, lc)
+               : plain_impl<false, true, false, false, false>(a, lc);
   }
   return launch_plain_other(a, lc);
 }

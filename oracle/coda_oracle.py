@@ -353,13 +353,29 @@ def ln_mlp_bwd_reparam(fwd, x, W0, W1, W2, gamma, beta, dout,
     sa = (dy @ w1) / d
     sb = (np.sum(dy * y, axis=1) - dy @ b1) / d
     dyhat = st(r[:, None] * dy)
+    nb = ln_norm_bwd_stage(dyhat, W1, h, gamma, beta, r, mu, sa, sb, store_bf16)
+    dh = nb["dh"]
+    return {"dy": dy, "sa": sa, "sb": sb, "dyhat": dyhat, "P": nb["P"], "dh": dh, "dz": dh,
+            "hhat": nb["hhat"], "dgamma": np.sum(nb["dgamma_rows"], axis=0),
+            "dbeta": np.sum(nb["dbeta_rows"], axis=0), "dW1": nb["hhat"].T @ dyhat,
+            "dW2": a.T @ dout, "dx": st(dh @ W0.T), "dW0": x.T @ dh}
+
+
+def ln_norm_bwd_stage(dyhat, W1, h, gamma, beta, r, mu, sa, sb, store_bf16: bool = False):
+    """The LayerNorm backward as the epilogue of P = dyhat W1^T (the last
+    step of ``ln_mlp_bwd_reparam``), on any subset of rows:
+        dh = gamma P - r s_a - r^2 s_b (h - mu)
+        hhat = (h - mu) gamma + beta / r
+    with the per-row terms of the weight gradients, dgamma_rows = P (h - mu)
+    and dbeta_rows = P / r (their column sums are dgamma, dbeta)."""
+    st = _store(store_bf16)
+    dyhat, W1, h, gamma, beta, r, mu, sa, sb = (np.asarray(t, dtype=f64) for t in
+                                                (dyhat, W1, h, gamma, beta, r, mu, sa, sb))
     P = dyhat @ W1.T
     hc = h - mu[:, None]
     dh = st(gamma[None, :] * P - (r * sa)[:, None] - (r * r * sb)[:, None] * hc)
     hhat = st(hc * gamma[None, :] + beta[None, :] / r[:, None])
-    return {"dy": dy, "sa": sa, "sb": sb, "dyhat": dyhat, "P": P, "dh": dh, "dz": dh,
-            "hhat": hhat, "dgamma": np.sum(P * hc, axis=0), "dbeta": np.sum(P / r[:, None], axis=0),
-            "dW1": hhat.T @ dyhat, "dW2": a.T @ dout, "dx": st(dh @ W0.T), "dW0": x.T @ dh}
+    return {"P": P, "dh": dh, "hhat": hhat, "dgamma_rows": P * hc, "dbeta_rows": P / r[:, None]}
 
 
 # --------------------------------------------------------------------------

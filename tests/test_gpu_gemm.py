@@ -67,6 +67,32 @@ def test_gemm_many_tiles_per_cta(coda, transA, transB):
     assert_close("gemm 4096^2 x 320", C, a @ b, 1e-5)
 
 
+@pytest.mark.parametrize("transA", [1, 0])
+@pytest.mark.parametrize("c_fp32", [1, 0])
+def test_gemm_two_slab_long_k(coda, transA, c_fp32):
+    """Long-K shapes that select the two-slab pair tile (512 rows per CTA
+    pair, two MMAs per K step sharing B; with 76 co-resident pairs, 152 such
+    tiles against 304 one-slab tiles): ragged M (4000 = 7.8 pair tiles), N
+    (4840 = 18.9 column tiles) and K (8232 = 128.6 k-blocks). Checked on a
+    row sample that includes every slab and pair-tile boundary."""
+    M, N, K = 4000, 4840, 8232
+    A = _rand((K, M) if transA else (M, K), 21)
+    B = _rand((K, N), 22)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32 if c_fp32 else torch.bfloat16,
+                   device="cuda")
+    coda.coda_gemm(A.cuda(), B.cuda(), C, transA=bool(transA))
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    rng = np.random.default_rng(23)
+    edges = [r for b in range(128, M, 128) for r in (b - 1, b)]
+    rows = np.array(sorted(set(rng.choice(M, 40, replace=False).tolist()) | set(edges) | {0, M - 1}))
+    a = to64(A).T[rows] if transA else to64(A)[rows]
+    ref = a @ to64(B)
+    got = C.cpu()[rows]
+    assert torch.isfinite(got.float()).all()
+    assert_close(f"two-slab gemm tA={transA} f32={c_fp32}", got, ref, 1e-5 if c_fp32 else TOL_BF16)
+
+
 def test_gemm_strided_operands(coda):
     # leading dimensions larger than the logical width (views into wider buffers)
     M, N, K = 136, 72, 96

@@ -6,6 +6,7 @@ r (hg W1) - (r mu) w1 + b1 with w1 = gamma W1, b1 = beta W1; the two
 LayerNorm-backward statistics are accumulated in the epilogue of the GEMM
 that produces dy, and the LayerNorm backward itself is fused into the GEMM
 producing dyhat W1^T. Every call goes through the C ABI."""
+import numpy as np
 import pytest
 import torch
 
@@ -93,3 +94,90 @@ def test_ln_stage_isolated_statistics(coda):
     assert_close("s_b (stage-isolated)", bw["sb"], sb["sb"], TOL_F32)
     assert_close("dh (stage-isolated)", bw["dh"], sb["dh"], TOL_BF16)
     assert_close("hhat (stage-isolated)", bw["hhat"], sb["hhat"], TOL_BF16)
+
+
+def _sample_rows(M, n, seed):
+    rng = np.random.default_rng(seed)
+    edges = [r for b in range(128, M, 128) for r in (b - 1, b)]
+    return np.array(sorted(set(rng.choice(M, n, replace=False).tolist()) | set(edges) | {0, M - 1}))
+
+
+def test_ln_norm_bwd_long_k(coda):
+    """The LayerNorm-backward GEMM at K = 2f = 8192 with 8192 rows (many
+    tiles per CTA pair, long K): dh and hhat on a row sample covering every
+    128-row and pair-tile edge, the dgamma / dbeta partials on 32-row blocks
+    around those edges, against the oracle's LayerNorm-backward stage."""
+    M, d, two_f = 8192, 2048, 8192
+    g = torch.Generator().manual_seed(64)
+    dyhat = (torch.randn(M, two_f, generator=g) * 0.05).to(torch.bfloat16)
+    W1 = (torch.randn(d, two_f, generator=g) * 0.02).to(torch.bfloat16)
+    h = torch.randn(M, d, generator=g).to(torch.bfloat16)
+    gamma = (torch.rand(d, generator=g) + 0.5).to(torch.bfloat16)
+    beta = (torch.randn(d, generator=g) * 0.3).to(torch.bfloat16)
+    r = torch.rand(M, generator=g) + 0.5
+    mu = torch.randn(M, generator=g) * 0.1
+    sa = torch.randn(M, generator=g) * 0.01
+    sb = torch.randn(M, generator=g) * 0.01
+    cu = {k: v.cuda() for k, v in dict(dyhat=dyhat, W1=W1, h=h, gamma=gamma, beta=beta, r=r,
+                                        mu=mu, sa=sa, sb=sb).items()}
+    dh = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
+    hhat = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
+    dgp = torch.empty(coda.row_tiles32(M), d, dtype=torch.float32, device="cuda")
+    dbp = torch.empty(coda.row_tiles32(M), d, dtype=torch.float32, device="cuda")
+    coda.coda_gemm_resid_ln_stats_bwd(cu["dyhat"], cu["W1"], cu["h"], cu["gamma"], cu["beta"],
+                                      cu["r"], cu["mu"], cu["sa"], cu["sb"], dh, dgp, dbp,
+                                      hhat=hhat)
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    rows = _sample_rows(M, 60, 65)
+    n = {k: O.to64(v) for k, v in dict(dyhat=dyhat, W1=W1, h=h, gamma=gamma, beta=beta, r=r,
+                                       mu=mu, sa=sa, sb=sb).items()}
+    ref = O.ln_norm_bwd_stage(n["dyhat"][rows], n["W1"], n["h"][rows], n["gamma"], n["beta"],
+                              n["r"][rows], n["mu"][rows], n["sa"][rows], n["sb"][rows],
+                              store_bf16=True)
+    assert_close("dh (long K)", dh.cpu()[rows], ref["dh"], TOL_BF16)
+    assert_close("hhat (long K)", hhat.cpu()[rows], ref["hhat"], TOL_BF16)
+    blocks = [0, 3, 4, 7, 8, 15, 16, 31, 32, 127, 128, M // 32 - 1]
+    brows = np.concatenate([np.arange(32 * j, 32 * j + 32) for j in blocks])
+    rb = O.ln_norm_bwd_stage(n["dyhat"][brows], n["W1"], n["h"][brows], n["gamma"], n["beta"],
+                             n["r"][brows], n["mu"][brows], n["sa"][brows], n["sb"][brows])
+    dg_ref = rb["dgamma_rows"].reshape(len(blocks), 32, d).sum(axis=1)
+    db_ref = rb["dbeta_rows"].reshape(len(blocks), 32, d).sum(axis=1)
+    # the fused path forms P from bf16 operands in fp32 like the oracle; the
+    # partials multiply it by the bf16-stored h: compare at the fp32 tolerance
+    assert_close("dgamma partials (long K)", dgp.cpu()[blocks], dg_ref, TOL_F32)
+    assert_close("dbeta partials (long K)", dbp.cpu()[blocks], db_ref, TOL_F32)
+
+
+@pytest.mark.parametrize("ln", [0, 1])
+def test_resid_stats_long_k(coda, ln):
+    """The residual + statistics GEMM at K = 8192 (e.g. a down projection
+    feeding the next norm) with 8192 rows: h, hg and the per-tile row
+    partials (sum h^2, and sum h for LayerNorm) on a row sample, against
+    h = x W + z in fp64."""
+    M, K, N = 8192, 8192, 2048
+    g = torch.Generator().manual_seed(66 + ln)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    W = (torch.randn(K, N, generator=g) * 0.02).to(torch.bfloat16)
+    z = torch.randn(M, N, generator=g).to(torch.bfloat16)
+    gamma = (torch.rand(N, generator=g) + 0.5).to(torch.bfloat16)
+    h = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    hg = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    psq = torch.empty(coda.col_tiles(N), M, dtype=torch.float32, device="cuda")
+    psum = torch.empty(coda.col_tiles(N), M, dtype=torch.float32, device="cuda")
+    if ln:
+        coda.coda_gemm_resid_ln_stats(x.cuda(), W.cuda(), z.cuda(), gamma.cuda(), h, hg, psq, psum)
+    else:
+        coda.coda_gemm_resid_norm_stats(x.cuda(), W.cuda(), z.cuda(), gamma.cuda(), h, hg, psq)
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    rows = _sample_rows(M, 60, 67)
+    href = O.to64(x)[rows] @ O.to64(W) + O.to64(z)[rows]
+    assert_close("h (long K)", h.cpu()[rows], href, TOL_BF16)
+    assert_close("hg (long K)", hg.cpu()[rows], href * O.to64(gamma)[None, :], TOL_BF16)
+    tiles = href.reshape(len(rows), -1, 256)
+    assert_close("sum h^2 partials (long K)", psq.cpu()[:, rows], (tiles ** 2).sum(axis=2).T,
+                 TOL_F32)
+    if ln:
+        assert_close("sum h partials (long K)", psum.cpu()[:, rows], tiles.sum(axis=2).T,
+                     TOL_F32)
