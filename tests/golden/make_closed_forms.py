@@ -4,7 +4,8 @@ from the oracle or from the CUDA library.
 
 Citations (page title, section):
   * ln V for all-zero logits: "Reading notes on CODA", s2 "Cross-entropy loss"
-    (l_i = -h_{i,y_i} + log sum_k exp h_{i,k}; with every logit 0 it is log V).
+    (l_i = -h_{i,y_i} + log sum_k exp h_{i,k}; with every logit 0 it is log V);
+    the same definition on eight bf16-exact logits (ce_exact8).
   * RoPE frequencies and rotations: "CODA: Rewriting Transformer Blocks as
     GEMM-Epilogue Programs" (pith.science), Fig. 7 caption (RoPE rotates each
     feature pair); theta = 500000 and head dim 128 are the Llama-3-8B-shaped
@@ -37,6 +38,12 @@ def main():
     out["ce_small"] = {"logits": ["0", "ln2", "ln3", "0"], "lse": f(mp.log(7)),
                        "loss_target2": f(mp.log(mp.mpf(7) / 3)),
                        "loss_target0": f(mp.log(7))}
+
+    # Eight logits that bf16 holds exactly: lse = ln sum exp, loss_t = lse - l_t.
+    lg = ["0", "1", "2", "0.5", "-1", "3", "0", "0.25"]
+    lse8 = mp.log(sum(mp.exp(mp.mpf(v)) for v in lg))
+    out["ce_exact8"] = {"logits": [float(v) for v in lg], "lse": f(lse8),
+                        "loss": [f(lse8 - mp.mpf(v)) for v in lg]}
 
     # RoPE inverse frequencies theta^(-2i/128), theta = 5e5.
     th = mp.mpf(500000)

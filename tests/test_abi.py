@@ -67,6 +67,8 @@ def test_invalid_arguments_rejected_on_host(L):
     # empty and negative sizes
     assert L.coda_gemm(ok, 64, 0, ok, 64, 0, None, None, ok, 64, 0, 0, 64, 64, None) == 1
     assert L.coda_gemm(ok, 64, 0, ok, 64, 0, None, None, ok, 64, 0, 64, -1, 64, None) == 1
+    # beyond the largest supported extent (2^30 - 1 per dimension)
+    assert L.coda_gemm(ok, 64, 0, ok, 64, 0, None, None, ok, 64, 0, 1 << 30, 64, 64, None) == 1
     # row stride not a multiple of 16 bytes
     assert L.coda_gemm(ok, 65, 0, ok, 64, 0, None, None, ok, 64, 0, 64, 64, 65, None) == 1
     # leading dimension smaller than the row

@@ -344,6 +344,14 @@ def test_ce_small_closed_form():
     assert abs(res["loss"][1] - g["loss_target0"]) < 1e-15
 
 
+def test_ce_exact8_closed_form():
+    g = GOLD["ce_exact8"]
+    W = np.array([g["logits"]])
+    res = O.lmhead_ce(np.ones((8, 1)), W, np.arange(8))
+    assert np.allclose(res["lse"], g["lse"], rtol=0, atol=1e-14)
+    assert np.allclose(res["loss"], g["loss"], rtol=0, atol=1e-14)
+
+
 def test_ce_brute_force_and_torch():
     rng = np.random.default_rng(10)
     hidden = rng.standard_normal((6, 5))
