@@ -514,7 +514,7 @@ def next_rows(step, flush, reps=5):
         ts.append(a.elapsed_time(b))
     ms = sorted(ts)[len(ts) // 2]
     fl = 3 * 2.0 * s2.M * s2.d * s2.V
-    chunk = min(4096, (s2.V + 255) // 256 * 256)
+    chunk = min(16384, (s2.V + 255) // 256 * 256)  # the recommended workspace's chunk
     rows = {"lmhead_ce_bwd": {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
                               "tokens_per_s": round(s2.M / (ms * 1e-3), 1),
                               "launches": 3 * ((s2.V + chunk - 1) // chunk)}}

@@ -19,7 +19,11 @@ cudaError_t launch_plain_other(const PlainArgs& a, const LaunchCtx& lc) {
   if (a.rowsq) return cudaErrorNotSupported;
   if (a.resid) {
     // C (+)= A B^T in fp32: e.g. a gradient accumulated over several launches
-    if (!a.a_mn && !a.b_mn && a.out_f32) return plain_t_impl<false, false, true, true>(a, lc);
+    if (!a.a_mn && !a.b_mn && a.out_f32) {
+      if (prefer_two_slabs(a.M, a.N, a.K, kTileN, lc.num_sms / 2))
+        return plain_t_impl<false, false, true, true, 2>(a, lc);
+      return plain_t_impl<false, false, true, true>(a, lc);
+    }
     return cudaErrorNotSupported;
   }
   if (!a.a_mn && !a.b_mn)

@@ -202,8 +202,10 @@ coda_status_t coda_lmhead_ce_noalloc(const void* hidden, const void* W, const in
                                      float* lse, float* loss, int M, int V, int d,
                                      coda_stream_t stream);
 
-/* Bytes of scratch that coda_lmhead_ce_bwd uses for M rows and V classes
- * (one bf16 gradient chunk of M x min(V rounded up to 256, 4096)). */
+/* Bytes of scratch that coda_lmhead_ce_bwd is designed for with M rows and V
+ * classes: one bf16 gradient chunk of M x min(V rounded up to 256, 16384)
+ * (268 MB at M = 8192). A smaller workspace (at least M * 256 * 2 bytes)
+ * gives narrower chunks; a larger one wider chunks, up to 32768 columns. */
 size_t coda_lmhead_ce_bwd_workspace_size(int M, int V);
 
 /* LM-head cross-entropy backward without materialising the logits

@@ -80,7 +80,8 @@ def test_ce_bwd_full_size(coda):
                           dl[rows].double().numpy())
     assert_close("dhidden (sampled rows)", bw["dhidden"].cpu()[rows], ref["dhidden"], TOL_BF16)
     cols = np.array(sorted(set(rng.choice(sh.V, 24, replace=False).tolist())
-                           | {0, 4095, 4096, sh.V - 1, int(inp["targets"][0])}))
+                           | {0, 4095, 4096, 16383, 16384, 114687, 114688, sh.V - 1,
+                              int(inp["targets"][0])}))
     dWc = O.lmhead_ce_dW_columns(O.to64(inp["hidden"]), Wd, inp["targets"].numpy(),
                                  dl.double().numpy(), cols)
     assert_close("dW (sampled columns)", bw["dW"].cpu()[:, cols], dWc, TOL_BF16)
