@@ -468,6 +468,10 @@ def run_coda(args):
     }
     if args.only:
         line["config"]["only"] = args.only
+    else:
+        line["per_config"] = per_config(step, per_call, peak)
+        line["aux_hbm"] = aux_hbm(step, per_call, peaks.get("hbm_gbs"))
+        line["l2_warm"] = l2_warm(step, args.steps, stream)
     if not args.only and not args.no_next_rows:
         line["next_rows"] = next_rows(step, flush)
     if not args.only and not args.no_unfused:
@@ -487,6 +491,68 @@ def run_coda(args):
 
 
 # ------------------------------------------------------------------ rows beyond the step
+
+def per_config(step, per_call, peak):
+    """The step's workloads one by one (sums of their calls' event times):
+    the 1B-shaped block forward and backward, the LM head + CE, the 8B-shaped
+    block forward + backward; GEMM FLOPs only."""
+    groups = {"llama1b_mlp_fwd": lambda n: n in ("1b.gemm_resid_norm_stats", "1b.row_rms",
+                                                    "1b.gemm_rowscale_swiglu", "1b.gemm_down"),
+              "lmhead_ce": lambda n: n == "lmhead_ce",
+              "llama1b_mlp_bwd": lambda n: n.startswith("1b.") and n not in (
+                  "1b.gemm_resid_norm_stats", "1b.row_rms", "1b.gemm_rowscale_swiglu",
+                  "1b.gemm_down"),
+              "llama8b_block_fwd_bwd": lambda n: n.startswith("8b.")}
+    out = {}
+    for gname, pred in groups.items():
+        ks = [k for k, c in enumerate(step.calls) if pred(c[0])]
+        if not ks:
+            continue
+        ms = sum(per_call[k] for k in ks)
+        fl = sum(step.calls[k][1] for k in ks)
+        ent = {"ms": round(ms, 4), "gflop": round(fl / 1e9, 1),
+               "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+               "frac_of_burst_peak": round(fl / (ms * 1e-3) / 1e12 / peak, 3)}
+        if gname == "lmhead_ce":
+            ent["tokens_per_s"] = round(step.s2.M / (ms * 1e-3), 1)
+        out[gname] = ent
+    return out
+
+
+def aux_hbm(step, per_call, hbm_gbs):
+    """The bandwidth-bound auxiliary kernels: algorithmic bytes / event time
+    against the measured copy bandwidth."""
+    out = {}
+    names = [c[0] for c in step.calls]
+    if "8b.rope_bwd" in names:
+        s4 = step.s4
+        M, N = s4.M, s4.n_qkv
+        # dqkv_rot bf16 and the fp16 saved copy in, dqkv_hat bf16 out, r in, s out,
+        # the cos/sin table once
+        byts = 3 * 2 * M * N + 8 * M + 4 * 2 * s4.seq_len * (s4.head_dim // 2)
+        ms = per_call[names.index("8b.rope_bwd")]
+        gbs = byts / (ms * 1e-3) / 1e9
+        out["rope_bwd"] = {"bytes": byts, "ms": round(ms, 4), "gb_s": round(gbs, 1),
+                           "frac_of_hbm_peak": round(gbs / hbm_gbs, 3) if hbm_gbs else None}
+    for n in ("1b.row_rms", "1b.row_rms_bwd", "1b.col_reduce"):
+        if n in names:
+            out[n.split(".", 1)[1] + "_us"] = round(1e3 * per_call[names.index(n)], 1)
+    return out
+
+
+def l2_warm(step, steps, stream):
+    """The same step back to back without the L2 flush in between (inputs and
+    weights partly L2-resident from the previous step)."""
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step.run()
+    b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"ms_per_step": round(ms, 4), "tflops": round(step.flops / (ms * 1e-3) / 1e12, 2)}
+
 
 def next_rows(step, flush, reps=5):
     """Kernels built beyond the step's rows, timed on the step's LM-head

@@ -140,6 +140,10 @@ bool map_f16_32(CUtensorMap* m, const void* p, int rows, int cols, int ld) {
   return tmap2d(m, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, cols, rows, ld, 32, 32,
                 CU_TENSOR_MAP_SWIZZLE_64B);
 }
+bool map_f16_64(CUtensorMap* m, const void* p, int rows, int cols, int ld) {
+  return tmap2d(m, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, cols, rows, ld, 64, 32,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+}
 bool map_f32_32(CUtensorMap* m, const void* p, int rows, int cols, int ld) {
   return tmap2d(m, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cols, rows, ld, 32, 32,
                 CU_TENSOR_MAP_SWIZZLE_128B);
@@ -509,8 +513,8 @@ coda_status_t coda_gemm_rowscale_swiglu_bwd(const void* dout, const void* W2, co
   SwiGLUBwdArgs p{};
   CHECK_MAP(map_a(&p.tmA, dout, d, 0, M, d));
   CHECK_MAP(map_b(&p.tmB, W2, d, 1, f, d));  // B[k, n] = W2[n, k]
-  CHECK_MAP(map_f16_32(&p.tm_y, y, M, 2 * f, 2 * f));
-  CHECK_MAP(map_bf16_32(&p.tm_dy, dyhat, M, 2 * f, 2 * f));
+  CHECK_MAP(map_f16_64(&p.tm_y, y, M, 2 * f, 2 * f));
+  CHECK_MAP(map_bf16_64(&p.tm_dy, dyhat, M, 2 * f, 2 * f));
   p.r = r;
   p.spart = spart;
   p.M = M;
@@ -702,8 +706,8 @@ coda_status_t coda_gemm_ln_rowscale_swiglu_bwd(const void* dout, const void* W2,
   SwiGLUBwdArgs p{};
   CHECK_MAP(map_a(&p.tmA, dout, d, 0, M, d));
   CHECK_MAP(map_b(&p.tmB, W2, d, 1, f, d));
-  CHECK_MAP(map_f16_32(&p.tm_y, y, M, 2 * f, 2 * f));
-  CHECK_MAP(map_bf16_32(&p.tm_dy, dyhat, M, 2 * f, 2 * f));
+  CHECK_MAP(map_f16_64(&p.tm_y, y, M, 2 * f, 2 * f));
+  CHECK_MAP(map_bf16_64(&p.tm_dy, dyhat, M, 2 * f, 2 * f));
   p.r = r;
   p.spart = spart;
   p.ln = 1;

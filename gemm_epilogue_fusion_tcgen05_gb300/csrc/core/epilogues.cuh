@@ -555,19 +555,19 @@ struct EpiCEGrad {
 // pith Fig. 7: the SwiGLU backward maps one incoming gradient to both paired
 // inputs; "Eliminating the RMSNorm backward kernel": the row statistic is
 // accumulated here):
-//   da = acc ; (g, u) = saved y pair (fp32) ; sg = sigmoid(g)
+//   da = acc ; (g, u) = saved y pair (fp16) ; sg = sigmoid(g)
 //   dg = da u sg (1 + g (1 - sg)) ; du = da g sg
 //   spart[nb, m] = sum (dg g + du u) ; dyhat = r (dg, du) (bf16)
-// Per 16-column chunk of da: one fp32 box of y (32 columns) in, one bf16 box
-// of dyhat (32 columns) out. A ring of kNL load slots keeps the y boxes of
-// the next kNL-1 chunks in flight; two store sets.
+// Per 32-column chunk of da: one fp16 box of y (64 columns, 128-byte rows)
+// in, one bf16 box of dyhat (64 columns) out. A ring of kNL load slots keeps
+// the y box of the next chunk in flight; two store sets.
 // With LN (LayerNorm variant) two more row partials for the relocated
 // LayerNorm statistics: spart_w = sum dy w1, spart_b = sum dy b1.
 template <bool LN>
 struct EpiSwiGLUBwd {
-  static constexpr int kYBufB = 2048;   // 32 rows x 32 fp16
-  static constexpr int kOBufB = 2048;   // 32 rows x 32 bf16
-  static constexpr int kNL = 3;
+  static constexpr int kYBufB = 4096;   // 32 rows x 64 fp16 (128-byte rows)
+  static constexpr int kOBufB = 4096;   // 32 rows x 64 bf16 (128-byte rows)
+  static constexpr int kNL = 2;
   static constexpr int kSmemPerWarp = kNL * kYBufB + 2 * kOBufB;
   struct Params {
     CUtensorMap tm_y, tm_dy;
@@ -586,12 +586,12 @@ struct EpiSwiGLUBwd {
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
                                                   int m0, int n0) {
-    for (int i = 0; i < kNL - 1; ++i) issue(p, c, c.cnt + i, 2 * (n0 + i * 16), m0);
+    for (int i = 0; i < kNL - 1; ++i) issue(p, c, c.cnt + i, 2 * (n0 + i * 32), m0);
   }
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
                                               int n0, int nb, uint32_t taddr) {
-    constexpr int NCH = BN / 16;
+    constexpr int NCH = BN / 32;
     const int row = m0 + 32 * c.q + c.lane;
     const float rr = row < g.M ? __ldg(p.r + row) : 0.f;
     float ss = 0.f, sw = 0.f, sb = 0.f;
@@ -600,44 +600,48 @@ struct EpiSwiGLUBwd {
       const uint32_t ybuf = c.buf + slot * kYBufB;
       const uint32_t obuf = c.buf + kNL * kYBufB + (c.cnt & 1) * kOBufB;
       c.stores_read_but_last();
-      if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, 2 * (n0 + (ch + kNL - 1) * 16), m0);
-      float da[16];
-      tmem_ld16(taddr + ch * 16, da);
-      float w[32], bb[32];
-      if constexpr (LN) {
-        load_nvec32f(p.w1, 2 * (n0 + ch * 16), 2 * g.N, w);
-        load_nvec32f(p.b1, 2 * (n0 + ch * 16), 2 * g.N, bb);
-      }
+      if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, 2 * (n0 + (ch + kNL - 1) * 32), m0);
+      float da[32];
+      tmem_ld32(taddr + ch * 32, da);
       if (!c.wait(slot, 12)) return false;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // output chunk k = pairs 4k .. 4k+3
-        const uint4 yv = ld_shared_v4(ybuf + swz<64>(c.lane, k));  // pairs 4k .. 4k+3
-        const float2 p0 = unpack_f16(yv.x), p1 = unpack_f16(yv.y), p2 = unpack_f16(yv.z),
-                     p3 = unpack_f16(yv.w);
-        const float gy[4] = {p0.x, p1.x, p2.x, p3.x};
-        const float uy[4] = {p0.y, p1.y, p2.y, p3.y};
-        uint32_t outw[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float gg = gy[t], uu = uy[t];
-          const float sg = sigmoidf_fast(gg);
-          const float d = da[4 * k + t];
-          const float dg = d * uu * sg * (1.0f + gg * (1.0f - sg));
-          const float du = d * gg * sg;
-          ss = fmaf(dg, gg, fmaf(du, uu, ss));
-          if constexpr (LN) {
-            const int q2 = 2 * (4 * k + t);
-            sw = fmaf(dg, w[q2], fmaf(du, w[q2 + 1], sw));
-            sb = fmaf(dg, bb[q2], fmaf(du, bb[q2 + 1], sb));
-          }
-          outw[t] = pack_bf16(rr * dg, rr * du);
+      for (int hh = 0; hh < 2; ++hh) {  // 16 pairs (32 y columns) at a time
+        float w[32], bb[32];
+        if constexpr (LN) {
+          load_nvec32f(p.w1, 2 * (n0 + ch * 32) + 32 * hh, 2 * g.N, w);
+          load_nvec32f(p.b1, 2 * (n0 + ch * 32) + 32 * hh, 2 * g.N, bb);
         }
-        st_shared_v4(obuf + swz<64>(c.lane, k), outw[0], outw[1], outw[2], outw[3]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // output 16-byte chunk k = pairs 4k .. 4k+3
+          const int k = 4 * hh + kk;
+          const uint4 yv = ld_shared_v4(ybuf + swz<128>(c.lane, k));
+          const float2 p0 = unpack_f16(yv.x), p1 = unpack_f16(yv.y), p2 = unpack_f16(yv.z),
+                       p3 = unpack_f16(yv.w);
+          const float gy[4] = {p0.x, p1.x, p2.x, p3.x};
+          const float uy[4] = {p0.y, p1.y, p2.y, p3.y};
+          uint32_t outw[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float gg = gy[t], uu = uy[t];
+            const float sg = sigmoidf_fast(gg);
+            const float d = da[4 * k + t];
+            const float dg = d * uu * sg * (1.0f + gg * (1.0f - sg));
+            const float du = d * gg * sg;
+            ss = fmaf(dg, gg, fmaf(du, uu, ss));
+            if constexpr (LN) {
+              const int q2 = 2 * (4 * kk + t);
+              sw = fmaf(dg, w[q2], fmaf(du, w[q2 + 1], sw));
+              sb = fmaf(dg, bb[q2], fmaf(du, bb[q2 + 1], sb));
+            }
+            outw[t] = pack_bf16(rr * dg, rr * du);
+          }
+          st_shared_v4(obuf + swz<128>(c.lane, k), outw[0], outw[1], outw[2], outw[3]);
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (c.lane == 0) {
-        c.store(&p.tm_dy, obuf, 2 * (n0 + ch * 16), m0 + 32 * c.q);
+        c.store(&p.tm_dy, obuf, 2 * (n0 + ch * 32), m0 + 32 * c.q);
         bulk_commit();
       }
       ++c.cnt;
