@@ -693,6 +693,46 @@ def unfused_reference(step, flush, steps=3, warmup=2):
     return tot / steps
 
 
+# ------------------------------------------------------------------ profiling cases
+
+# Reduced shapes of the step's kernels (a few GB on the device at most) for
+# multi-pass ncu captures; each runs 2 warm-up launches and 1 more launch.
+KERNEL_CASES = {
+    # weight gradient dW = X^T dY (both operands MN-major, fp32 out), K = tokens
+    "wgrad_4096x7168x16384": dict(M=4096, N=7168, K=16384, transA=True, f32=True),
+    # the forward-like GEMM with the same FLOPs (A K-major, B MN-major, bf16 out)
+    "fwd_16384x7168x4096": dict(M=16384, N=7168, K=4096, transA=False, f32=False),
+}
+
+
+def run_kernel_case(args):
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__ as g
+    g.build()
+    import gemm_epilogue_fusion_tcgen05_gb300 as C
+    cs = KERNEL_CASES[args.kernel_case]
+    gen = torch.Generator(device=dev).manual_seed(0)
+    M, N, K = cs["M"], cs["N"], cs["K"]
+    A = torch.randn((K, M) if cs["transA"] else (M, K), generator=gen, device=dev).to(torch.bfloat16)
+    B = torch.randn((K, N), generator=gen, device=dev).to(torch.bfloat16)
+    Cm = torch.empty((M, N), dtype=torch.float32 if cs["f32"] else torch.bfloat16, device=dev)
+    for _ in range(2):
+        C.coda_gemm(A, B, Cm, transA=cs["transA"])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    C.coda_gemm(A, B, Cm, transA=cs["transA"])
+    b.record()
+    b.synchronize()
+    st = C.get_device_error()
+    if st != 0:
+        raise SystemExit(f"device error {st}")
+    ms = a.elapsed_time(b)
+    print(json.dumps({"kernel_case": args.kernel_case, "ms": round(ms, 4),
+                      "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)}))
+
+
 # ------------------------------------------------------------------ primitive microbenchmarks
 
 def run_primitives(args):
@@ -862,6 +902,8 @@ def main():
     ap.add_argument("--no-8b", action="store_true", help="leave the 8B-shaped block out of the step")
     ap.add_argument("--primitives", action="store_true",
                     help="epilogue-primitive microbenchmarks instead of the step")
+    ap.add_argument("--kernel-case", default="", choices=[""] + sorted(KERNEL_CASES),
+                    help="run one reduced-shape GEMM three times (for ncu captures)")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the rows timed beyond the step (CE backward, LayerNorm block)")
     ap.add_argument("--no-unfused", action="store_true",
@@ -872,7 +914,9 @@ def main():
     if args.warmup < 3:
         print("note: at least 3 warm-up steps are required; using 3", file=sys.stderr)
         args.warmup = 3
-    if args.primitives:
+    if args.kernel_case:
+        run_kernel_case(args)
+    elif args.primitives:
         run_primitives(args)
     elif args.impl == "reference":
         run_reference(args)
