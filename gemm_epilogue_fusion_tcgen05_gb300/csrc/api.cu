@@ -238,10 +238,8 @@ coda_status_t coda_gemm(const void* A, int lda, int transA, const void* B, int l
   CHECK_MAP(map_b(&a.tmB, B, ldb, transB, N, K));
   if (c_fp32) CHECK_MAP(map_f32_32(&a.tmC, C, M, N, ldc));
   else CHECK_MAP(map_bf16_32(&a.tmC, C, M, N, ldc));
-  if (resid) {
-    if (c_fp32) CHECK_MAP(map_f32_32(&a.tmR, resid, M, N, ldc));
-    else CHECK_MAP(map_bf16_32(&a.tmR, resid, M, N, ldc));
-  }
+  a.resid_ptr = resid;
+  a.ld_res = (size_t)ldc * (c_fp32 ? 4 : 2);
   a.a_mn = transA != 0;
   a.b_mn = transB == 0;
   a.out_f32 = c_fp32 != 0;
@@ -271,7 +269,7 @@ coda_status_t coda_gemm_resid_norm_stats(const void* x, const void* W0, const vo
   ResidNormStatsArgs a{};
   CHECK_MAP(map_a(&a.tmA, x, K, 0, M, K));
   CHECK_MAP(map_b(&a.tmB, W0, N, 0, N, K));
-  CHECK_MAP(map_bf16_32(&a.tm_z, z, M, N, N));
+  a.z = static_cast<const bf16*>(z);
   CHECK_MAP(map_bf16_32(&a.tm_h, h, M, N, N));
   CHECK_MAP(map_bf16_32(&a.tm_hg, hg, M, N, N));
   a.gamma = static_cast<const bf16*>(gamma);
@@ -332,7 +330,7 @@ coda_status_t coda_gemm_rope(const void* A, const void* W, const float* r, const
   CHECK(M > 0 && N > 0 && K > 0 && M < kMaxDim && N < kMaxDim && K < kMaxDim,
         "coda_gemm_rope: bad sizes");
   CHECK(N % 8 == 0 && K % 8 == 0, "coda_gemm_rope: N and K must be multiples of 8");
-  CHECK(seq_len > 0 && head_dim > 0 && head_dim % 32 == 0, "coda_gemm_rope: head_dim % 32 != 0");
+  CHECK(seq_len > 0 && head_dim > 0 && head_dim % 32 == 0, "coda_gemm_rope: head_dim must be a positive multiple of 32");
   CHECK(n_rope_cols >= 0 && n_rope_cols <= N && n_rope_cols % head_dim == 0,
         "coda_gemm_rope: n_rope_cols must be a multiple of head_dim and <= N");
   TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
@@ -470,7 +468,8 @@ coda_status_t coda_lmhead_ce_bwd(const void* hidden, const void* W, const int32_
     CHECK_MAP(tmap2d(&h.tmB, Wb + v0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vc, d, V, 64,
                      kTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B));
     CHECK_MAP(map_f32_32(&h.tmC, dhidden, M, d, d));
-    if (v0 > 0) CHECK_MAP(map_f32_32(&h.tmR, dhidden, M, d, d));
+    h.resid_ptr = v0 > 0 ? dhidden : nullptr;
+    h.ld_res = (size_t)d * 4;
     h.a_mn = false;
     h.b_mn = false;
     h.out_f32 = true;
@@ -554,15 +553,13 @@ coda_status_t coda_gemm_resid_norm_stats_bwd(const void* dyhat, const void* W1, 
   NormBwdArgs p{};
   CHECK_MAP(map_a(&p.tmA, dyhat, two_f, 0, M, two_f));
   CHECK_MAP(map_b(&p.tmB, W1, two_f, 1, d, two_f));  // B[k, n] = W1[n, k]
-  CHECK_MAP(map_bf16_32(&p.tm_h, h, M, d, d));
   CHECK_MAP(map_bf16_32(&p.tm_dh, dh, M, d, d));
-  if (dresid) CHECK_MAP(map_bf16_32(&p.tm_dres, dresid, M, d, d));
-  else p.tm_dres = p.tm_h;  // unused
+  p.h = static_cast<const bf16*>(h);
+  p.dres = static_cast<const bf16*>(dresid);
   p.gamma = static_cast<const bf16*>(gamma);
   p.r = r;
   p.s = s;
   p.dgpart = dgamma_part;
-  p.has_dres = dresid != nullptr;
   p.M = M;
   p.N = d;
   p.K = two_f;
@@ -621,7 +618,7 @@ coda_status_t coda_gemm_resid_ln_stats(const void* x, const void* W0, const void
   ResidNormStatsArgs a{};
   CHECK_MAP(map_a(&a.tmA, x, K, 0, M, K));
   CHECK_MAP(map_b(&a.tmB, W0, N, 0, N, K));
-  CHECK_MAP(map_bf16_32(&a.tm_z, z, M, N, N));
+  a.z = static_cast<const bf16*>(z);
   CHECK_MAP(map_bf16_32(&a.tm_h, h, M, N, N));
   CHECK_MAP(map_bf16_32(&a.tm_hg, hg, M, N, N));
   a.gamma = static_cast<const bf16*>(gamma);
@@ -764,12 +761,11 @@ coda_status_t coda_gemm_resid_ln_stats_bwd(const void* dyhat, const void* W1, co
   NormBwdArgs p{};
   CHECK_MAP(map_a(&p.tmA, dyhat, two_f, 0, M, two_f));
   CHECK_MAP(map_b(&p.tmB, W1, two_f, 1, d, two_f));
-  CHECK_MAP(map_bf16_32(&p.tm_h, h, M, d, d));
   CHECK_MAP(map_bf16_32(&p.tm_dh, dh, M, d, d));
-  if (dresid) CHECK_MAP(map_bf16_32(&p.tm_dres, dresid, M, d, d));
-  else p.tm_dres = p.tm_h;  // unused
+  p.h = static_cast<const bf16*>(h);
+  p.dres = static_cast<const bf16*>(dresid);
   if (hhat) CHECK_MAP(map_bf16_32(&p.tm_hhat, hhat, M, d, d));
-  else p.tm_hhat = p.tm_h;  // unused
+  else p.tm_hhat = p.tm_dh;  // unused
   p.gamma = static_cast<const bf16*>(gamma);
   p.beta = static_cast<const bf16*>(beta);
   p.r = r;
@@ -778,7 +774,6 @@ coda_status_t coda_gemm_resid_ln_stats_bwd(const void* dyhat, const void* W1, co
   p.mu = mu;
   p.dgpart = dgamma_part;
   p.dbpart = dbeta_part;
-  p.has_dres = dresid != nullptr;
   p.save_hhat = hhat != nullptr;
   p.ln = 1;
   p.M = M;

@@ -55,6 +55,38 @@ __device__ __forceinline__ void load_nvec32f(const float* p, int n, int N, float
   }
 }
 
+// 16 * NV consecutive bytes of one row of a row-major tensor, starting at
+// byte `col_bytes` (a multiple of 16) of the row, read straight into
+// registers with 16-byte non-coherent loads: an epilogue's input tile, read
+// one chunk ahead of its use instead of being staged in shared memory. Rows
+// >= M and bytes at or past `row_bytes` read as zero; a vector that the row
+// ends inside is filled 2 bytes at a time, so nothing past the row's last
+// element is read (row strides are multiples of 16 bytes, row lengths of 2).
+template <int NV>
+__device__ __forceinline__ void ldg_row(const void* base, size_t ld_bytes, int row, int M,
+                                        int col_bytes, int row_bytes, uint4 (&o)[NV]) {
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) o[k] = zero;
+  if (row >= M) return;
+  const char* rp = static_cast<const char*>(base) + (size_t)row * ld_bytes;
+  const uint4* p = reinterpret_cast<const uint4*>(rp + col_bytes);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int b0 = col_bytes + 16 * k;
+    if (b0 + 16 <= row_bytes) {
+      o[k] = __ldg(p + k);
+    } else if (b0 < row_bytes) {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      const unsigned short* hp = reinterpret_cast<const unsigned short*>(rp + b0);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (b0 + 2 * e < row_bytes) w[e >> 1] |= (uint32_t)__ldg(hp + e) << (16 * (e & 1));
+      o[k] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 // Unpack one 16-byte chunk (8 bf16) from shared memory into o[0..7].
 __device__ __forceinline__ void unpack8(uint4 u, float* o) {
   o[0] = bf16_lo(u.x); o[1] = bf16_hi(u.x); o[2] = bf16_lo(u.y); o[3] = bf16_hi(u.y);
@@ -130,61 +162,56 @@ __device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
 // fp32 pre-image. fp32 output rows are 128 bytes per 32 columns, bf16 64;
 // the residual has the output's type (an fp32 residual may be C itself:
 // C += A B).
-// Two store sets; with a residual, a ring of kNL load slots keeps the
-// residual boxes of the next kNL-1 chunks in flight.
+// Two store sets; the residual is read straight into registers one chunk
+// ahead.
 template <bool OUT_F32, bool RESID, bool ROWSQ>
 struct EpiPlain {
   static constexpr int kRowB = OUT_F32 ? 128 : 64;
   static constexpr int kBufB = 32 * kRowB;
-  static constexpr int kNL = RESID ? (OUT_F32 ? 3 : 4) : 0;  // load slots, one box each
-  static constexpr int kLoadB = kBufB;  // the residual has the output's type
-  static constexpr int kSmemPerWarp = kNL * kLoadB + 2 * kBufB;
+  static constexpr int kNV = kRowB / 16;  // 16-byte vectors per row per chunk
+  static constexpr int kSmemPerWarp = 2 * kBufB;
   struct Params {
     CUtensorMap tm_c;
-    CUtensorMap tm_r;
+    const void* resid;    // [M, N] with the output's type, row stride ld_res bytes
+    size_t ld_res;
     float* rowsq;  // [tiles_n, M] when ROWSQ
   };
-  static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int n,
-                                               int m0) {
-    const int slot = k % kNL;
-    c.load(&p.tm_r, slot, c.buf + slot * kLoadB, n, m0 + 32 * c.q, kLoadB);
-  }
   template <int BN>
-  static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
-                                                  int m0, int n0) {
-    if constexpr (RESID) {
-      for (int i = 0; i < kNL - 1; ++i) issue(p, c, c.cnt + i, n0 + i * 32, m0);
-    }
-  }
+  static __device__ __forceinline__ void prefetch(const Params&, EpiCtx&, const GemmArgs&, int, int) {}
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
                                               int n0, int nb, uint32_t taddr) {
     constexpr int NCH = BN / 32;
+    constexpr int ESZ = OUT_F32 ? 4 : 2;
+    const int row = m0 + 32 * c.q + c.lane;
     float ss = 0.f;
+    uint4 rn[kNV] = {};
+    if constexpr (RESID) ldg_row<kNV>(p.resid, p.ld_res, row, g.M, ESZ * n0, ESZ * g.N, rn);
     for (int ch = 0; ch < NCH; ++ch) {
-      const uint32_t buf = c.buf + kNL * kLoadB + (c.cnt & 1) * kBufB;
-      c.stores_read_but_last();
+      uint4 rv[kNV];
+#pragma unroll
+      for (int k = 0; k < kNV; ++k) rv[k] = rn[k];
       if constexpr (RESID) {
-        if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, n0 + (ch + kNL - 1) * 32, m0);
+        if (ch + 1 < NCH)
+          ldg_row<kNV>(p.resid, p.ld_res, row, g.M, ESZ * (n0 + (ch + 1) * 32), ESZ * g.N, rn);
       }
+      const uint32_t buf = c.buf + (c.cnt & 1) * kBufB;
+      c.stores_read_but_last();
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
       if constexpr (RESID) {
-        const int slot = c.cnt % kNL;
-        if (!c.wait(slot, 10)) return false;
-        const uint32_t lb = c.buf + slot * kLoadB;
         if constexpr (OUT_F32) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint4 u = ld_shared_v4(lb + swz<128>(c.lane, k));
-            v[4 * k] += __uint_as_float(u.x);
-            v[4 * k + 1] += __uint_as_float(u.y);
-            v[4 * k + 2] += __uint_as_float(u.z);
-            v[4 * k + 3] += __uint_as_float(u.w);
+            v[4 * k] += __uint_as_float(rv[k].x);
+            v[4 * k + 1] += __uint_as_float(rv[k].y);
+            v[4 * k + 2] += __uint_as_float(rv[k].z);
+            v[4 * k + 3] += __uint_as_float(rv[k].w);
           }
         } else {
           float z[32];
-          read_bf16x32(lb, c.lane, z);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) unpack8(rv[k], &z[8 * k]);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] += z[j];
         }
@@ -211,7 +238,6 @@ struct EpiPlain {
       ++c.cnt;
     }
     if constexpr (ROWSQ) {
-      const int row = m0 + 32 * c.q + c.lane;
       if (row < g.M) p.rowsq[(size_t)nb * g.M + row] = ss;
     }
     return true;
@@ -224,46 +250,44 @@ struct EpiPlain {
 // unscaled D, side output D * gamma[n]):
 //   h = acc + z (stored), hg = h * gamma (stored), part[nb, m] = sum_n h^2
 // With LN (the LayerNorm variant) also part2[nb, m] = sum_n h.
-// A ring of kNL load slots keeps the z boxes of the next kNL-1 chunks in
-// flight; two store sets of {h, hg}.
+// z is read straight into registers one chunk ahead (no shared-memory
+// staging, which leaves room for pipeline stages); two store sets of {h, hg}.
 template <bool LN>
 struct EpiResidNormStats {
   static constexpr int kBufB = 2048;  // 32 rows x 32 bf16
-  static constexpr int kNL = 4;
   static constexpr int kStoreB = 2 * kBufB;
-  static constexpr int kSmemPerWarp = kNL * kBufB + 2 * kStoreB;
+  static constexpr int kSmemPerWarp = 2 * kStoreB;
   struct Params {
-    CUtensorMap tm_z, tm_h, tm_hg;
+    CUtensorMap tm_h, tm_hg;
+    const __nv_bfloat16* z;  // [M, N] residual, read into registers a chunk ahead
     const __nv_bfloat16* gamma;
     float* part;   // [tiles_n, M] sums of h^2
     float* part2;  // [tiles_n, M] sums of h (LN only)
   };
-  static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int n,
-                                               int m0) {
-    const int slot = k % kNL;
-    c.load(&p.tm_z, slot, c.buf + slot * kBufB, n, m0 + 32 * c.q, kBufB);
-  }
   template <int BN>
-  static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
-                                                  int m0, int n0) {
-    for (int i = 0; i < kNL - 1; ++i) issue(p, c, c.cnt + i, n0 + i * 32, m0);
-  }
+  static __device__ __forceinline__ void prefetch(const Params&, EpiCtx&, const GemmArgs&, int, int) {}
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
                                               int n0, int nb, uint32_t taddr) {
     constexpr int NCH = BN / 32;
+    const int row = m0 + 32 * c.q + c.lane;
+    const size_t ldb = (size_t)g.N * 2;
     float ss = 0.f, s1 = 0.f;
+    uint4 zn[4];
+    ldg_row<4>(p.z, ldb, row, g.M, 2 * n0, 2 * g.N, zn);
     for (int ch = 0; ch < NCH; ++ch) {
-      const int slot = c.cnt % kNL;
-      const uint32_t hbuf = c.buf + kNL * kBufB + (c.cnt & 1) * kStoreB;
+      uint4 zv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) zv[k] = zn[k];
+      if (ch + 1 < NCH) ldg_row<4>(p.z, ldb, row, g.M, 2 * (n0 + (ch + 1) * 32), 2 * g.N, zn);
+      const uint32_t hbuf = c.buf + (c.cnt & 1) * kStoreB;
       const uint32_t gbuf = hbuf + kBufB;
       c.stores_read_but_last();
-      if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, n0 + (ch + kNL - 1) * 32, m0);
       float v[32], gm[32], z[32];
       tmem_ld32(taddr + ch * 32, v);
       load_nvec32(p.gamma, n0 + ch * 32, g.N, gm);
-      if (!c.wait(slot, 11)) return false;
-      read_bf16x32(c.buf + slot * kBufB, c.lane, z);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) unpack8(zv[k], &z[8 * k]);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         v[j] += z[j];
@@ -282,7 +306,6 @@ struct EpiResidNormStats {
       }
       ++c.cnt;
     }
-    const int row = m0 + 32 * c.q + c.lane;
     if (row < g.M) {
       p.part[(size_t)nb * g.M + row] = ss;
       if constexpr (LN) p.part2[(size_t)nb * g.M + row] = s1;
@@ -667,40 +690,29 @@ struct EpiSwiGLUBwd {
 //   optional side output hhat = (h - mu) gamma + beta / r, the operand of
 //   the W1 weight gradient (dW1 = hhat^T dyhat).
 // The column sums use a warp transpose-reduce; partials are per 32 rows.
-// A ring of kNL load slots of {h, dres} boxes runs kNL-1 chunks ahead; two
-// store sets of dh (and hhat).
+// h and dres are read straight into registers one chunk ahead; two store
+// sets of dh (and hhat).
 template <bool LN>
 struct EpiNormBwd {
   static constexpr int kBufB = 2048;
-  static constexpr int kNL = 3;
-  static constexpr int kLoadB = 2 * kBufB;
   static constexpr int kStoreB = (LN ? 2 : 1) * kBufB;
-  static constexpr int kSmemPerWarp = kNL * kLoadB + 2 * kStoreB;
+  static constexpr int kSmemPerWarp = 2 * kStoreB;
   struct Params {
-    CUtensorMap tm_h, tm_dres, tm_dh, tm_hhat;
+    CUtensorMap tm_dh, tm_hhat;
+    const __nv_bfloat16* h;         // [M, N], read into registers a chunk ahead
+    const __nv_bfloat16* dres;      // nullable, [M, N], likewise
     const __nv_bfloat16* gamma;
     const float* r;
     const float* s;                 // s (RMSNorm) or s_b (LN)
     float* dgpart;                  // [ceil(M/32), N]
-    int has_dres;
     const float* mu;                // LN only
     const float* sa;                // LN only
     const __nv_bfloat16* beta;      // LN only
     float* dbpart;                  // LN only, [ceil(M/32), N]
     int save_hhat;                  // LN only
   };
-  static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int n,
-                                               int m0) {
-    const int slot = k % kNL;
-    const uint32_t base = c.buf + slot * kLoadB;
-    c.load(&p.tm_h, slot, base, n, m0 + 32 * c.q, kBufB);
-    if (p.has_dres) c.load(&p.tm_dres, kNL + slot, base + kBufB, n, m0 + 32 * c.q, kBufB);
-  }
   template <int BN>
-  static __device__ __forceinline__ void prefetch(const Params& p, EpiCtx& c, const GemmArgs&,
-                                                  int m0, int n0) {
-    for (int i = 0; i < kNL - 1; ++i) issue(p, c, c.cnt + i, n0 + i * 32, m0);
-  }
+  static __device__ __forceinline__ void prefetch(const Params&, EpiCtx&, const GemmArgs&, int, int) {}
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
                                               int n0, int, uint32_t taddr) {
@@ -717,18 +729,30 @@ struct EpiNormBwd {
       rinv = live ? 1.0f / rr : 0.f;
     }
     const int prow = (m0 >> 5) + c.q;  // partial row (32 rows each)
+    const size_t ldb = (size_t)g.N * 2;
+    const bool has_dres = p.dres != nullptr;
+    uint4 hn[4], rn[4] = {};
+    ldg_row<4>(p.h, ldb, row, g.M, 2 * n0, 2 * g.N, hn);
+    if (has_dres) ldg_row<4>(p.dres, ldb, row, g.M, 2 * n0, 2 * g.N, rn);
     for (int ch = 0; ch < NCH; ++ch) {
-      const int slot = c.cnt % kNL;
-      const uint32_t hbuf = c.buf + slot * kLoadB;
-      const uint32_t rbuf = hbuf + kBufB;
-      const uint32_t obuf = c.buf + kNL * kLoadB + (c.cnt & 1) * kStoreB;
+      uint4 hv[4], rv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        hv[k] = hn[k];
+        rv[k] = rn[k];
+      }
+      if (ch + 1 < NCH) {
+        const int cb = 2 * (n0 + (ch + 1) * 32);
+        ldg_row<4>(p.h, ldb, row, g.M, cb, 2 * g.N, hn);
+        if (has_dres) ldg_row<4>(p.dres, ldb, row, g.M, cb, 2 * g.N, rn);
+      }
+      const uint32_t obuf = c.buf + (c.cnt & 1) * kStoreB;
       c.stores_read_but_last();
-      if (ch + kNL - 1 < NCH) issue(p, c, c.cnt + kNL - 1, n0 + (ch + kNL - 1) * 32, m0);
       float P[32], h[32], gm[32];
       tmem_ld32(taddr + ch * 32, P);
       load_nvec32(p.gamma, n0 + ch * 32, g.N, gm);
-      if (!c.wait(slot, 13)) return false;
-      read_bf16x32(hbuf, c.lane, h);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) unpack8(hv[k], &h[8 * k]);
       if constexpr (LN) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) h[j] -= mu;  // h - mu from here on
@@ -736,10 +760,10 @@ struct EpiNormBwd {
       float dh[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) dh[j] = gm[j] * P[j] - k2 * h[j] - k1;
-      if (p.has_dres) {
-        if (!c.wait(kNL + slot, 14)) return false;
+      if (has_dres) {
         float rz[32];
-        read_bf16x32(rbuf, c.lane, rz);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) unpack8(rv[k], &rz[8 * k]);
 #pragma unroll
         for (int j = 0; j < 32; ++j) dh[j] += rz[j];
       }

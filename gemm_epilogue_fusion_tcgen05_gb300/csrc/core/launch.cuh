@@ -62,8 +62,10 @@ inline void choose_tile_order(GemmArgs& g, int bm, int bn, int K, int conc) {
 // K = 8192 with 7 one-slab waves against 4 two-slab waves they measured even).
 constexpr int kTwoSlabMinK = 8192;
 constexpr double kTwoSlabCost = 0.80;
+constexpr double kEpiKbLoads = 24.0;  // epilogues that also read tiles (residual, h)
+constexpr int kTwoSlabMinKLoads = 12288;  // ... which measured no gain at K = 8192
 inline bool prefer_two_slabs(int M, int N, int K, int bn, int pairs, double epi_kb = 16.0) {
-  if (K < kTwoSlabMinK || pairs <= 0) return false;
+  if (K < (epi_kb > 16.0 ? kTwoSlabMinKLoads : kTwoSlabMinK) || pairs <= 0) return false;
   const double tn = (double)((N + bn - 1) / bn);
   const double t1 = (double)((M + 255) / 256) * tn, t2 = (double)((M + 511) / 512) * tn;
   const double w1 = std::ceil(t1 / pairs), w2 = std::ceil(t2 / pairs);

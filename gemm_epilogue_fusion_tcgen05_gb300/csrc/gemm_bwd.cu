@@ -25,20 +25,19 @@ cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
   return a.ln ? swiglu_bwd_impl<true>(a, lc) : swiglu_bwd_impl<false>(a, lc);
 }
 
-template <bool LN>
+template <bool LN, int MS>
 static cudaError_t norm_bwd_impl(const NormBwdArgs& a, const LaunchCtx& lc) {
   using E = EpiNormBwd<LN>;
-  using T = Gemm2Traits<kTileN, false, false, E>;
+  using T = Gemm2Traits<kTileN, false, false, E, MS>;
   typename E::Params p{};
-  p.tm_h = a.tm_h;
-  p.tm_dres = a.tm_dres;
+  p.h = a.h;
+  p.dres = a.dres;
   p.tm_dh = a.tm_dh;
   p.tm_hhat = a.tm_hhat;
   p.gamma = a.gamma;
   p.r = a.r;
   p.s = a.s;
   p.dgpart = a.dgpart;
-  p.has_dres = a.has_dres;
   p.mu = a.mu;
   p.sa = a.sa;
   p.beta = a.beta;
@@ -48,9 +47,10 @@ static cudaError_t norm_bwd_impl(const NormBwdArgs& a, const LaunchCtx& lc) {
 }
 
 cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc) {
-  // one slab even though K = 2f is long: with this epilogue's staging two
-  // slabs leave three 48 KiB stages and measured no faster
-  return a.ln ? norm_bwd_impl<true>(a, lc) : norm_bwd_impl<false>(a, lc);
+  // K = 2f is long: two-slab tiles where the wave count allows
+  if (prefer_two_slabs(a.M, a.N, a.K, kTileN, lc.num_sms / 2, kEpiKbLoads))
+    return a.ln ? norm_bwd_impl<true, 2>(a, lc) : norm_bwd_impl<false, 2>(a, lc);
+  return a.ln ? norm_bwd_impl<true, 1>(a, lc) : norm_bwd_impl<false, 1>(a, lc);
 }
 
 }  // namespace coda

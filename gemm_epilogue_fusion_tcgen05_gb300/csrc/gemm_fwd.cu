@@ -5,12 +5,12 @@
 
 namespace coda {
 
-template <bool LN>
+template <bool LN, int MS>
 static cudaError_t resid_norm_stats_impl(const ResidNormStatsArgs& a, const LaunchCtx& lc) {
   using E = EpiResidNormStats<LN>;
-  using T = Gemm2Traits<kTileN, false, true, E>;
+  using T = Gemm2Traits<kTileN, false, true, E, MS>;
   typename E::Params p{};
-  p.tm_z = a.tm_z;
+  p.z = a.z;
   p.tm_h = a.tm_h;
   p.tm_hg = a.tm_hg;
   p.gamma = a.gamma;
@@ -20,9 +20,10 @@ static cudaError_t resid_norm_stats_impl(const ResidNormStatsArgs& a, const Laun
 }
 
 cudaError_t launch_resid_norm_stats(const ResidNormStatsArgs& a, const LaunchCtx& lc) {
-  // one slab even for long K: with this epilogue's 64 KiB of staging, two
-  // slabs leave three 48 KiB stages and measured no faster
-  return a.ln ? resid_norm_stats_impl<true>(a, lc) : resid_norm_stats_impl<false>(a, lc);
+  // long K (e.g. the down projection feeding the next norm): two-slab tiles
+  if (prefer_two_slabs(a.M, a.N, a.K, kTileN, lc.num_sms / 2, kEpiKbLoads))
+    return a.ln ? resid_norm_stats_impl<true, 2>(a, lc) : resid_norm_stats_impl<false, 2>(a, lc);
+  return a.ln ? resid_norm_stats_impl<true, 1>(a, lc) : resid_norm_stats_impl<false, 1>(a, lc);
 }
 
 template <bool LN>

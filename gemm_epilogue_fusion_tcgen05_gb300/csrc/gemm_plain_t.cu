@@ -10,7 +10,8 @@ static cudaError_t plain_t_impl(const PlainArgs& a, const LaunchCtx& lc) {
   using T = Gemm2Traits<kTileN, AMN, BMN, E, MS>;
   typename E::Params p{};
   p.tm_c = a.tmC;
-  p.tm_r = a.tmR;
+  p.resid = a.resid_ptr;
+  p.ld_res = a.ld_res;
   p.rowsq = nullptr;
   return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }

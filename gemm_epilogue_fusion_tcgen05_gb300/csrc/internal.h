@@ -20,15 +20,18 @@ struct LaunchCtx {
 
 // Plain GEMM: C = op(A) op(B) (+ resid), optional per-row sum of squares.
 struct PlainArgs {
-  CUtensorMap tmA, tmB, tmC, tmR;
+  CUtensorMap tmA, tmB, tmC;
   bool a_mn, b_mn, out_f32, resid, rowsq;
+  const void* resid_ptr;   // [M, N] with the output's type (read by the epilogue without TMA)
+  size_t ld_res;           // its row stride in bytes
   float* rowsq_part;
   int M, N, K;
 };
 cudaError_t launch_plain(const PlainArgs& a, const LaunchCtx& lc);
 
 struct ResidNormStatsArgs {
-  CUtensorMap tmA, tmB, tm_z, tm_h, tm_hg;
+  CUtensorMap tmA, tmB, tm_h, tm_hg;
+  const bf16* z;   // [M, N] residual (read by the epilogue without TMA)
   const bf16* gamma;
   float* part;
   int M, N, K;
@@ -91,12 +94,13 @@ struct SwiGLUBwdArgs {
 cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc);
 
 struct NormBwdArgs {
-  CUtensorMap tmA, tmB, tm_h, tm_dres, tm_dh, tm_hhat;
+  CUtensorMap tmA, tmB, tm_dh, tm_hhat;
+  const bf16* h;      // [M, N] (read by the epilogue without TMA)
+  const bf16* dres;   // nullable [M, N]
   const bf16* gamma;
   const float* r;
   const float* s;
   float* dgpart;
-  int has_dres;
   int M, N, K;
   int ln;        // LayerNorm variant (s is s_b)
   const float* mu;

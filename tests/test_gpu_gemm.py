@@ -119,6 +119,39 @@ def test_gemm_resid_rowsq(coda, MNK):
     assert_close("row sum of squares", part.sum(0), np.sum(ref * ref, axis=1), 1e-3)
 
 
+@pytest.mark.parametrize("c_fp32", [0, 1])
+def test_gemm_resid_row_ends_inside_a_vector(coda, c_fp32):
+    """The epilogue reads the residual straight into registers, 16 bytes at a
+    time; here each row ends inside such a vector (N = 260 bf16 / 262 fp32,
+    inside row strides of 264 elements), so the last elements come from the
+    partial-vector path."""
+    M, K = 200, 72
+    N = 262 if c_fp32 else 260
+    dt = torch.float32 if c_fp32 else torch.bfloat16
+    A, Bbig = _rand((M, K), 17), _rand((K, 264), 18, 0.1)
+    B = Bbig[:, :N]  # row stride 264 elements (16-byte multiple)
+    g = torch.Generator().manual_seed(19)
+    Rbig = torch.full((M, 264), float("nan"), dtype=dt)
+    Rbig[:, :N] = torch.randn(M, N, generator=g).to(dt)
+    Cbig = torch.zeros((M, 264), dtype=dt, device="cuda")
+    Rd = Rbig.cuda()
+    if c_fp32:  # C += A B: the residual is C itself
+        Cbig[:, :N] = Rd[:, :N]
+        coda.coda_gemm(A.cuda(), Bbig.cuda()[:, :N], Cbig[:, :N], resid=Cbig[:, :N])
+    else:
+        Rv = Rd[:, :N]
+        Cv = Cbig[:, :N]
+        assert Rv.stride() == Cv.stride()
+        coda.coda_gemm(A.cuda(), Bbig.cuda()[:, :N], Cv, resid=Rv)
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    ref = to64(A) @ to64(B) + to64(Rbig[:, :N])
+    assert_close(f"gemm+resid, ragged vector (f32={c_fp32})", Cbig[:, :N], ref,
+                 1e-5 if c_fp32 else TOL_BF16)
+    assert_close("last columns", Cbig[:, N - 4:N], ref[:, N - 4:], 1e-5 if c_fp32 else TOL_BF16)
+    assert torch.all(Cbig[:, N:] == 0), "wrote outside the logical columns"
+
+
 def test_bounded_wait_gives_up_without_fault(coda):
     st = coda.coda_selftest_bounded_wait(20)
     assert st == coda.CODA_ERR_TIMEOUT
