@@ -4,9 +4,15 @@
 // Each CTA stages its own 128 rows of A and half (BN/2 columns) of B, so per
 // SM the shared-memory traffic per MMA and the operand bytes fetched from L2
 // are half those of a single-CTA 128 x BN tile; TMEM of each CTA holds its
-// 128 accumulator rows. The epilogue is unchanged: every CTA's four epilogue
-// warps drain their own 128 x BN slice (same epilogue classes as the
-// single-CTA kernel).
+// 128 accumulator rows; every CTA's four epilogue warps drain their own
+// 128 x BN slice. Two TMEM accumulator buffers let the MMA warp fill buffer
+// b^1 while the epilogue warps drain buffer b (the sm_103a counterpart of the
+// pages' Hopper PingPong overlap).
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: this CTA's A rows and B half into a ring of stages
+//   warp 1      TMEM allocator; in the even CTA, the single thread issuing tcgen05.mma
+//   warps 2..5  epilogue: TMEM -> registers -> epilogue math -> smem -> TMA store
 //
 // Synchronisation across the pair:
 //   full[s]   (even CTA)  both CTAs' TMA loads complete_tx here; the even

@@ -73,37 +73,7 @@ inline bool prefer_two_slabs(int M, int N, int K, int bn, int pairs, double epi_
   return w2 * (2.0 * kTwoSlabCost + epi_kb / kblocks) < 0.97 * w1;
 }
 
-template <class T>
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                        const typename T::Epi::Params& ep, int M, int N, int K, const LaunchCtx& lc) {
-  static std::atomic<unsigned long long> attr_set{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_set.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(gemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             T::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set.fetch_or(bit, std::memory_order_acq_rel);
-  }
-  GemmArgs g;
-  g.M = M;
-  g.N = N;
-  g.K = K;
-  g.tiles_m = (M + kBM - 1) / kBM;
-  g.tiles_n = (N + T::BN - 1) / T::BN;
-  g.num_tiles = g.tiles_m * g.tiles_n;
-  g.num_kb = (K + kBK - 1) / kBK;
-  choose_tile_order(g, kBM, T::BN, K, g.num_tiles < lc.num_sms ? g.num_tiles : lc.num_sms);
-  g.err = lc.err;
-  g.timeout_ns = lc.timeout_ns;
-  const int grid = g.num_tiles < lc.num_sms ? g.num_tiles : lc.num_sms;
-  gemm_kernel<T><<<grid, T::kThreads, T::SMEM_BYTES, lc.stream>>>(tmA, tmB, ep, g);
-  return cudaGetLastError();
-}
-
-// CTA-pair variant: clusters of 2, grid = 2 x min(tiles, co-resident pairs).
+// Launch of the CTA-pair kernel: clusters of 2, grid = 2 x min(tiles, co-resident pairs).
 template <class T>
 cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const typename T::Epi::Params& ep, int M, int N, int K, const LaunchCtx& lc) {
