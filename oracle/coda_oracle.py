@@ -38,7 +38,6 @@ unpinned for that comparison only.
 """
 from __future__ import annotations
 
-import math
 from typing import Dict, Optional
 
 import numpy as np
@@ -654,7 +653,3 @@ def to64(t) -> np.ndarray:
         return t.detach().to(torch.float64).cpu().numpy()
     return np.asarray(t, dtype=f64)
 
-
-def lse_closed_form_zero_weights(V: int) -> float:
-    """With W = 0 every logit is 0, so LSE = log V and loss = log V."""
-    return math.log(V)

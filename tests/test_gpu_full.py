@@ -4,7 +4,8 @@ benchmark times (same entry points, same shapes):
   * Llama-3-1B-shaped block forward (M=8192, d=2048, f=8192): every output
     on sampled rows against the oracle (rows are independent in the forward).
   * LM head + CE (8192 x 2048 x 128256): LSE and loss on sampled rows.
-  * backward of the 1B block: every output against the full fp64 oracle.
+  * backward of the 1B block: every output against the full fp64 oracle;
+    the same for the LayerNorm variant of the block.
   * Llama-3-8B-shaped block forward + backward (M=16384, d=4096, f=14336):
     per-row outputs on sampled rows; weight gradients through the property
     dW v = A^T (G v) for random v (A, G the GPU's own saved operands, which
@@ -14,7 +15,8 @@ import numpy as np
 import pytest
 import torch
 
-from coda_inputs import WORKLOADS, mlp_block_inputs, lmhead_inputs, block8b_inputs, positions
+from coda_inputs import (WORKLOADS, BlockShape, mlp_block_inputs, ln_block_inputs, lmhead_inputs,
+                         block8b_inputs, positions)
 from oracle import coda_oracle as O
 from tests._util import TOL_BF16, TOL_F32, TOL_S_EXACT, assert_close, to64
 
@@ -91,6 +93,40 @@ def test_llama1b_backward_full_oracle(coda):
     sb = O.mlp_bwd_reparam(st, n["x"], n["W0"], n["W1"], n["W2"], n["gamma"], n["dout"],
                            store_bf16=True, stat_only=True)
     assert_close("s (storage-rounded oracle)", bw["s"], sb["s"], TOL_F32)
+
+
+def test_llama1b_layernorm_block_full_oracle(coda):
+    """The LayerNorm variant at the Llama-3-1B MLP shape (M = 8192, d = 2048,
+    f = 8192, seed 8), forward and backward, every output against the full
+    fp64 canonical oracle; s_a, s_b also against the storage-rounded
+    rewritten oracle."""
+    from gemm_epilogue_fusion_tcgen05_gb300 import blocks
+    sh = BlockShape("llama1b_ln_mlp", M=8192, d=2048, f=8192, seed=8)
+    inp = ln_block_inputs(sh)
+    g = {k: v.cuda() for k, v in inp.items()}
+    fw = blocks.ln_mlp_block_fwd(g["x"], g["z"], g["W0"], g["W1"], g["W2"], g["gamma"], g["beta"])
+    bw = blocks.ln_mlp_block_bwd(fw, g["x"], g["W0"], g["W1"], g["W2"], g["gamma"], g["beta"],
+                                 g["dout"])
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    n = {k: O.to64(v) for k, v in inp.items()}
+    args = (n["x"], n["z"], n["W0"], n["W1"], n["W2"], n["gamma"], n["beta"])
+    ref = O.ln_mlp_fwd(*args)
+    for k in ("h", "y", "a", "out"):
+        assert_close(k, fw[k], ref[k], TOL_BF16)
+    assert_close("mu", fw["mu"], ref["mu"], TOL_F32)
+    assert_close("r", fw["r"], ref["r"], TOL_F32)
+    rb = O.ln_mlp_bwd(ref, n["x"], n["W0"], n["W1"], n["W2"], n["gamma"], n["beta"], n["dout"])
+    for k in ("dx", "dz", "dW0", "dW1", "dW2", "dgamma", "dbeta"):
+        assert_close(k, bw[k], rb[k], TOL_BF16)
+    assert_close("s_a (exact oracle)", bw["sa"], rb["sa"], TOL_S_EXACT)
+    assert_close("s_b (exact oracle)", bw["sb"], rb["sb"], TOL_S_EXACT)
+    del ref, rb
+    st = O.ln_mlp_fwd_reparam(*args, store_bf16=True)
+    sb = O.ln_mlp_bwd_reparam(st, n["x"], n["W0"], n["W1"], n["W2"], n["gamma"], n["beta"],
+                              n["dout"], store_bf16=True)
+    assert_close("s_a (storage-rounded oracle)", bw["sa"], sb["sa"], TOL_F32)
+    assert_close("s_b (storage-rounded oracle)", bw["sb"], sb["sb"], TOL_F32)
 
 
 def _proj_check(name, dW, A, G, seed):
