@@ -361,8 +361,6 @@ def run_coda(args):
         raise SystemExit(f"device error after warm-up: {st}")
 
     n = len(step.calls)
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-            for _ in range(n)] for _ in range(args.steps)]
     step_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
                for _ in range(args.steps)]
     clocks = Clocks(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
@@ -376,7 +374,7 @@ def run_coda(args):
     for i in range(args.steps):
         flush.fill_(float(i))
         step_ev[i][0].record(stream)
-        step.run(evs[i])
+        step.run()  # no events between the calls: consecutive kernels overlap (PDL)
         step_ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -389,13 +387,26 @@ def run_coda(args):
 
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     ms = sum(step_ms) / len(step_ms)
-    per_call = [0.0] * n
-    for i in range(args.steps):
-        for k in range(n):
-            per_call[k] += evs[i][k][0].elapsed_time(evs[i][k][1])
-    per_call = [t / args.steps for t in per_call]
     ms = max_over_ranks(ms, dev)
     value = job_throughput(step.flops, ws, ms)
+
+    # per-call attribution: a separate pass with an event pair around every
+    # call. The events serialise the calls (no launch overlap), so this pass
+    # is not the timed one; it gives each kernel's own duration.
+    n_attr = max(2, min(args.steps, 5))
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in range(n)] for _ in range(n_attr)]
+    attr_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+               for _ in range(n_attr)]
+    for i in range(n_attr):
+        flush.fill_(float(i))
+        attr_ev[i][0].record(stream)
+        step.run(evs[i])
+        attr_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    per_call = [sum(evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(n_attr)) / n_attr
+                for k in range(n)]
+    attr_ms = sum(a.elapsed_time(b) for a, b in attr_ev) / n_attr
 
     # end-to-end through the public API with host buffers: copy this step's
     # inputs host -> device from pinned memory, run, read the results back
@@ -465,6 +476,9 @@ def run_coda(args):
                           "only before its first reader"},
         "clocks": clk,
         "parts_ms": {step.calls[k][0]: round(per_call[k], 4) for k in range(n)},
+        "parts_note": ("per-call CUDA-event times from a separate pass with events between "
+                       f"the calls (that pass: {attr_ms:.4f} ms/step; the timed steps have no "
+                       "events between calls, so consecutive kernels overlap their launch)"),
     }
     if args.only:
         line["config"]["only"] = args.only
@@ -702,6 +716,10 @@ KERNEL_CASES = {
     "wgrad_4096x7168x16384": dict(M=4096, N=7168, K=16384, transA=True, f32=True),
     # the forward-like GEMM with the same FLOPs (A K-major, B MN-major, bf16 out)
     "fwd_16384x7168x4096": dict(M=16384, N=7168, K=4096, transA=False, f32=False),
+    # the row-scale + RoPE GEMM of the 8B block at half its rows (bf16 out + fp16 copy)
+    "rope_8192x6144x4096": dict(M=8192, N=6144, K=4096, kind="rope"),
+    # the plain GEMM of the same shape, for comparison
+    "fwd_8192x6144x4096": dict(M=8192, N=6144, K=4096, transA=False, f32=False),
 }
 
 
@@ -714,15 +732,26 @@ def run_kernel_case(args):
     cs = KERNEL_CASES[args.kernel_case]
     gen = torch.Generator(device=dev).manual_seed(0)
     M, N, K = cs["M"], cs["N"], cs["K"]
-    A = torch.randn((K, M) if cs["transA"] else (M, K), generator=gen, device=dev).to(torch.bfloat16)
-    B = torch.randn((K, N), generator=gen, device=dev).to(torch.bfloat16)
-    Cm = torch.empty((M, N), dtype=torch.float32 if cs["f32"] else torch.bfloat16, device=dev)
+    if cs.get("kind") == "rope":
+        from gemm_epilogue_fusion_tcgen05_gb300 import blocks
+        A = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
+        B = (torch.randn((K, N), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+        r = torch.rand(M, generator=gen, device=dev) + 0.5
+        table = blocks.rope_table(4096, 128, 500000.0, dev)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        save = torch.empty((M, N), dtype=torch.float16, device=dev)
+        fn = lambda: C.coda_gemm_rope(A, B, r, table, 4096, 128, N - 1024, out, save)
+    else:
+        A = torch.randn((K, M) if cs["transA"] else (M, K), generator=gen, device=dev).to(torch.bfloat16)
+        B = torch.randn((K, N), generator=gen, device=dev).to(torch.bfloat16)
+        Cm = torch.empty((M, N), dtype=torch.float32 if cs["f32"] else torch.bfloat16, device=dev)
+        fn = lambda: C.coda_gemm(A, B, Cm, transA=cs["transA"])
     for _ in range(2):
-        C.coda_gemm(A, B, Cm, transA=cs["transA"])
+        fn()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    C.coda_gemm(A, B, Cm, transA=cs["transA"])
+    fn()
     b.record()
     b.synchronize()
     st = C.get_device_error()

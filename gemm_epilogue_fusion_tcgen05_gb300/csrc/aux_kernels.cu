@@ -18,6 +18,7 @@ namespace coda {
 // r[m] = 1 / sqrt(sum_j part[j, m] * inv_d + eps)
 __global__ void row_rms_kernel(const float* __restrict__ part, int nparts, int M, float inv_d,
                                float eps, float* __restrict__ r) {
+  grid_dep_wait();  // the producer of our inputs has finished (no-op without PDL)
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
   float acc = 0.f;
@@ -36,6 +37,7 @@ __global__ void row_rms_kernel(const float* __restrict__ part, int nparts, int M
 // out[m] = scale * sum_j part[j, m]
 __global__ void row_sum_scale_kernel(const float* __restrict__ part, int nparts, int M, float scale,
                                      float* __restrict__ out) {
+  grid_dep_wait();  // the producer of our inputs has finished (no-op without PDL)
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
   float acc = 0.f;
@@ -47,6 +49,7 @@ __global__ void row_sum_scale_kernel(const float* __restrict__ part, int nparts,
 // the 8 rows of threads stride over j, then combine through shared memory.
 __global__ void col_reduce_kernel(const float* __restrict__ part, int nparts, int N,
                                   float* __restrict__ out) {
+  grid_dep_wait();  // the producer of our inputs has finished (no-op without PDL)
   __shared__ float sm[8][33];
   const int n = blockIdx.x * 32 + threadIdx.x;
   float acc = 0.f;
@@ -68,6 +71,7 @@ __global__ void ce_combine_kernel(const float2* __restrict__ part, int nparts,
                                   const float* __restrict__ tlogit, const int* __restrict__ targets,
                                   int M, int V, float* __restrict__ lse, float* __restrict__ loss,
                                   int* err) {
+  grid_dep_wait();  // the producer of our inputs has finished (no-op without PDL)
   __shared__ float smax[8][33], ssum[8][33];
   const int m = blockIdx.x * 32 + threadIdx.x;
   float mx = -INFINITY, sm = 0.f;
@@ -107,6 +111,7 @@ __global__ void ce_combine_kernel(const float2* __restrict__ part, int nparts,
 // cos_sin[p, i] = (cos(p theta_i), sin(p theta_i)), theta_i = theta^(-2i/hd),
 // evaluated in fp64 and rounded to fp32.
 __global__ void rope_table_kernel(float2* __restrict__ cs, int seq_len, int head_dim, double theta) {
+  grid_dep_wait();  // the producer of our inputs has finished (no-op without PDL)
   const int half = head_dim / 2;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= seq_len * half) return;
@@ -128,6 +133,7 @@ __global__ void rope_bwd_kernel(const __nv_bfloat16* __restrict__ d, const __hal
                                 const float* __restrict__ r, const float2* __restrict__ cs,
                                 int seq_len, int head_dim, int n_rope, __nv_bfloat16* __restrict__ out,
                                 float* __restrict__ s, int M, int N, float inv_d) {
+  grid_dep_wait();  // the producer of our inputs has finished (no-op without PDL)
   const int m = blockIdx.x;
   if (m >= M) return;
   const float rr = r ? __ldg(r + m) : 1.f;
@@ -187,6 +193,7 @@ __global__ void rope_bwd_kernel(const __nv_bfloat16* __restrict__ d, const __hal
 __global__ void ln_stats_kernel(const float* __restrict__ psq, const float* __restrict__ psum,
                                 int nparts, int M, float inv_d, float eps, float* __restrict__ r,
                                 float* __restrict__ mu) {
+  grid_dep_wait();  // the producer of our inputs has finished (no-op without PDL)
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
   float a = 0.f, b = 0.f;
@@ -205,6 +212,7 @@ __global__ void ln_stats_kernel(const float* __restrict__ psq, const float* __re
 __global__ void ln_bwd_stats_kernel(const float* __restrict__ sp, const float* __restrict__ spw,
                                     const float* __restrict__ spb, int nparts, int M, float inv_d,
                                     float* __restrict__ sa, float* __restrict__ sb) {
+  grid_dep_wait();  // the producer of our inputs has finished (no-op without PDL)
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
   float y = 0.f, w = 0.f, b = 0.f;
@@ -236,47 +244,63 @@ __global__ void bounded_wait_probe_kernel(int* err, unsigned long long timeout_n
 }
 
 // ------------------------------------------------------------------ launchers
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel in the stream drains and waits for it in
+// grid_dep_wait(). These kernels never release their own dependents early
+// (their grids can span several waves), so nothing can crowd them out.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_row_rms(const float* part, int nparts, int M, float inv_d, float eps, float* r,
                            cudaStream_t st) {
-  row_rms_kernel<<<(M + 255) / 256, 256, 0, st>>>(part, nparts, M, inv_d, eps, r);
-  return cudaGetLastError();
+  return launch_pdl(row_rms_kernel, dim3((M + 255) / 256), dim3(256), st, part, nparts, M, inv_d, eps, r);
 }
 cudaError_t launch_row_sum_scale(const float* part, int nparts, int M, float scale, float* out,
                                  cudaStream_t st) {
-  row_sum_scale_kernel<<<(M + 255) / 256, 256, 0, st>>>(part, nparts, M, scale, out);
-  return cudaGetLastError();
+  return launch_pdl(row_sum_scale_kernel, dim3((M + 255) / 256), dim3(256), st, part, nparts, M, scale,
+                    out);
 }
 cudaError_t launch_col_reduce(const float* part, int nparts, int N, float* out, cudaStream_t st) {
-  col_reduce_kernel<<<(N + 31) / 32, dim3(32, 8), 0, st>>>(part, nparts, N, out);
-  return cudaGetLastError();
+  return launch_pdl(col_reduce_kernel, dim3((N + 31) / 32), dim3(32, 8), st, part, nparts, N, out);
 }
 cudaError_t launch_ce_combine(const float2* part, int nparts, const float* tlogit, const int* targets,
                               int M, int V, float* lse, float* loss, int* err, cudaStream_t st) {
-  ce_combine_kernel<<<(M + 31) / 32, dim3(32, 8), 0, st>>>(part, nparts, tlogit, targets, M, V, lse,
-                                                           loss, err);
-  return cudaGetLastError();
+  return launch_pdl(ce_combine_kernel, dim3((M + 31) / 32), dim3(32, 8), st, part, nparts, tlogit,
+                    targets, M, V, lse, loss, err);
 }
 cudaError_t launch_rope_table(float2* cs, int seq_len, int head_dim, double theta, cudaStream_t st) {
   const int n = seq_len * (head_dim / 2);
-  rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(cs, seq_len, head_dim, theta);
-  return cudaGetLastError();
+  return launch_pdl(rope_table_kernel, dim3((n + 255) / 256), dim3(256), st, cs, seq_len, head_dim,
+                    theta);
 }
 cudaError_t launch_rope_bwd(const __nv_bfloat16* d, const __half* q, const float* r,
                             const float2* cs, int seq_len, int head_dim, int n_rope,
                             __nv_bfloat16* out, float* s, int M, int N, float inv_d, cudaStream_t st) {
-  rope_bwd_kernel<<<M, 128, 0, st>>>(d, q, r, cs, seq_len, head_dim, n_rope, out, s, M, N, inv_d);
-  return cudaGetLastError();
+  return launch_pdl(rope_bwd_kernel, dim3(M), dim3(128), st, d, q, r, cs, seq_len, head_dim, n_rope,
+                    out, s, M, N, inv_d);
 }
 cudaError_t launch_ln_stats(const float* part_sq, const float* part_sum, int nparts, int M, float inv_d,
                             float eps, float* r, float* mu, cudaStream_t st) {
-  ln_stats_kernel<<<(M + 255) / 256, 256, 0, st>>>(part_sq, part_sum, nparts, M, inv_d, eps, r, mu);
-  return cudaGetLastError();
+  return launch_pdl(ln_stats_kernel, dim3((M + 255) / 256), dim3(256), st, part_sq, part_sum, nparts,
+                    M, inv_d, eps, r, mu);
 }
 cudaError_t launch_ln_bwd_stats(const float* spart, const float* spart_w, const float* spart_b,
                                 int nparts, int M, float inv_d, float* sa, float* sb, cudaStream_t st) {
-  ln_bwd_stats_kernel<<<(M + 255) / 256, 256, 0, st>>>(spart, spart_w, spart_b, nparts, M, inv_d,
-                                                       sa, sb);
-  return cudaGetLastError();
+  return launch_pdl(ln_bwd_stats_kernel, dim3((M + 255) / 256), dim3(256), st, spart, spart_w,
+                    spart_b, nparts, M, inv_d, sa, sb);
 }
 cudaError_t launch_bounded_wait_probe(int* err, unsigned long long timeout_ns, cudaStream_t st) {
   bounded_wait_probe_kernel<<<1, 32, 0, st>>>(err, timeout_ns);

@@ -121,6 +121,12 @@ __global__ void __launch_bounds__(T::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const DevError e{g.err, abort_flag, g.timeout_ns};
+  // everything above (barriers, TMEM, descriptor prefetch) may overlap the
+  // previous kernel's drain; no global memory is touched before this wait.
+  // All of this grid's CTAs are resident (grid <= co-resident clusters), so
+  // the next kernel's CTAs, once released, only take SMs ours have left.
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)

@@ -83,16 +83,20 @@ cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
   if (e != cudaSuccess) return e;
   dev &= 63;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the kernel's prologue may overlap the
+  // previous kernel's drain (the kernel waits in grid_dep_wait())
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(T::kThreads, 1, 1);
   cfg.dynamicSmemBytes = T::SMEM_BYTES;
   cfg.stream = lc.stream;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
   int pairs_max = max_pairs[dev].load(std::memory_order_acquire);
   if (pairs_max <= 0) {
     e = cudaFuncSetAttribute(gemm2_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -120,6 +124,7 @@ cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
   g.err = lc.err;
   g.timeout_ns = lc.timeout_ns;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, gemm2_kernel<T>, tmA, tmB, ep, g);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -37,6 +37,14 @@ __device__ __forceinline__ void flag_error(const DevError& e, int code, int wher
   if (e.word) atomicCAS(e.word, 0, (code & 0xff) | (where << 8));
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream drains;
+// grid_dep_wait() blocks until that kernel has completed and its memory
+// operations are visible (a no-op for a kernel launched without the
+// attribute). grid_dep_launch() lets the next kernel start launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
