@@ -102,11 +102,6 @@ __device__ __forceinline__ void stage_bf16x32(uint32_t buf, int lane, const floa
                  pack_bf16(v[8 * k + 6], v[8 * k + 7]));
 }
 
-__device__ __forceinline__ void read_bf16x32(uint32_t buf, int lane, float (&v)[32]) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) unpack8(ld_shared_v4(buf + swz<64>(lane, k)), &v[8 * k]);
-}
-
 // fp16 pair packing (round to nearest); the low half holds `lo`.
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
