@@ -486,6 +486,7 @@ def run_coda(args):
         line["per_config"] = per_config(step, per_call, peak)
         line["aux_hbm"] = aux_hbm(step, per_call, peaks.get("hbm_gbs"))
         line["l2_warm"] = l2_warm(step, args.steps, stream)
+        line["graph"] = graph_step(step, flush, args.steps, stream)
     if not args.only and not args.no_next_rows:
         line["next_rows"] = next_rows(step, flush)
     if not args.only and not args.no_unfused:
@@ -566,6 +567,25 @@ def l2_warm(step, steps, stream):
     b.synchronize()
     ms = a.elapsed_time(b) / steps
     return {"ms_per_step": round(ms, 4), "tflops": round(step.flops / (ms * 1e-3) / 1e12, 2)}
+
+
+def graph_step(step, flush, steps, stream):
+    """The same step captured once into a CUDA graph (blocks.CapturedStep)
+    and replayed, L2 flushed before each replay: one host launch per step."""
+    from gemm_epilogue_fusion_tcgen05_gb300 import blocks
+    cap = blocks.CapturedStep(step.run, warmup=1)
+    ts = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        cap.replay()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = sum(ts) / len(ts)
+    return {"ms_per_step": round(ms, 4), "tflops": round(step.flops / (ms * 1e-3) / 1e12, 2),
+            "what": "the timed step captured once in a CUDA graph and replayed"}
 
 
 def next_rows(step, flush, reps=5):

@@ -79,8 +79,12 @@ int coda_row_tiles32(int M);
 void coda_set_timeout_ms(int ms);
 
 /* Synchronises `stream`, then returns and clears the device error word:
- * CODA_OK, CODA_ERR_TIMEOUT (a bounded wait ran out) or
- * CODA_ERR_INVALID_VALUE (a CE target outside [0, V)). */
+ * CODA_OK, CODA_ERR_TIMEOUT (a bounded wait ran out),
+ * CODA_ERR_INVALID_VALUE (a CE target outside [0, V)) or CODA_ERR_RANGE (a
+ * value beyond the fp16 range in a saved fp16 copy). There is one error word
+ * per device, shared by every stream and thread: it holds the first error
+ * recorded since it was last read, and reading it clears it, so callers that
+ * launch on several streams of one device should read it from one place. */
 coda_status_t coda_get_device_error(coda_stream_t stream);
 
 /* Text of the last error seen by this thread (never NULL). */
