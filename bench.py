@@ -460,6 +460,8 @@ def run_coda(args):
                    "l2": "flushed before each step (512 MiB write, outside the step events)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "pct_bf16_peak": round(100 * value / ws / peak, 2),
+        "pct_bf16_sustained_peak": (round(100 * value / ws / peaks["bf16_tflops_sustained"], 2)
+                                    if peaks.get("bf16_tflops_sustained") else None),
         "lmhead_ce_tokens_per_s": round(lm_tok_s, 1) if lm_tok_s else None,
         "gpu_launches": step.launches_per_step * args.steps,
         "wall_s_timed_region": round(wall, 4),
@@ -467,6 +469,8 @@ def run_coda(args):
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{src} bf16_tflops (burst: the timed region is short "
                                     "and runs at the maximum SM clock)",
+                     "frac_of_sustained_peak": (round(achieved / peaks["bf16_tflops_sustained"], 4)
+                                                if peaks.get("bf16_tflops_sustained") else None),
                      "flops_per_launch": fl, "ms_per_launch": round(per_call[k_dom], 4),
                      "traffic": traffic},
         "e2e": {"value": round(e2e_value, 2) if e2e_value else None, "unit": UNIT,
@@ -475,6 +479,8 @@ def run_coda(args):
                 "copies": "per input group on a copy stream; compute waits for a group "
                           "only before its first reader"},
         "clocks": clk,
+        "step_ms_spread": {"min": round(min(step_ms), 4), "median": round(sorted(step_ms)[len(step_ms) // 2], 4),
+                           "max": round(max(step_ms), 4), "all": [round(t, 3) for t in step_ms]},
         "parts_ms": {step.calls[k][0]: round(per_call[k], 4) for k in range(n)},
         "parts_note": ("per-call CUDA-event times from a separate pass with events between "
                        f"the calls (that pass: {attr_ms:.4f} ms/step; the timed steps have no "
