@@ -54,14 +54,23 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def _smi_id(local: int) -> str:
+    """nvidia-smi's name for this process's CUDA device `local` (its UUID, so
+    that CUDA_VISIBLE_DEVICES renumbering does not matter)."""
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        return str(local)
+
+
 class Clocks:
     """Samples nvidia-smi every 200 ms while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
+    def __init__(self, gpu_id: str):
+        self.idx = gpu_id
         self.proc = None
         self.lines = []
 
@@ -363,8 +372,7 @@ def run_coda(args):
     n = len(step.calls)
     step_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
                for _ in range(args.steps)]
-    clocks = Clocks(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
-                    if False else local)
+    clocks = Clocks(_smi_id(local))
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -746,6 +754,9 @@ KERNEL_CASES = {
     "rope_8192x6144x4096": dict(M=8192, N=6144, K=4096, kind="rope"),
     # the plain GEMM of the same shape, for comparison
     "fwd_8192x6144x4096": dict(M=8192, N=6144, K=4096, transA=False, f32=False),
+    # the 1B block's SwiGLU GEMM at half its rows (a bf16 + the fp16 saved y)
+    "swiglu_4096x16384x2048": dict(M=4096, N=16384, K=2048, kind="swiglu"),
+    "fwd_4096x16384x2048": dict(M=4096, N=16384, K=2048, transA=False, f32=False),
 }
 
 
@@ -758,7 +769,14 @@ def run_kernel_case(args):
     cs = KERNEL_CASES[args.kernel_case]
     gen = torch.Generator(device=dev).manual_seed(0)
     M, N, K = cs["M"], cs["N"], cs["K"]
-    if cs.get("kind") == "rope":
+    if cs.get("kind") == "swiglu":
+        A = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
+        B = (torch.randn((K, N), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+        r = torch.rand(M, generator=gen, device=dev) + 0.5
+        a_out = torch.empty((M, N // 2), dtype=torch.bfloat16, device=dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        fn = lambda: C.coda_gemm_rowscale_swiglu(A, B, r, a_out, y)
+    elif cs.get("kind") == "rope":
         from gemm_epilogue_fusion_tcgen05_gb300 import blocks
         A = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
         B = (torch.randn((K, N), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
