@@ -20,6 +20,7 @@ __device__ int g_coda_err;  // device error word, one per device
 
 thread_local std::string t_last_error;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<int> g_multicast{0};
 
 coda_status_t fail(coda_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 coda_status_t fail(coda_status_t s, const char* fmt, ...) {
@@ -111,8 +112,8 @@ bool tmap2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
 }
 
 // Operand maps for the mainloop: 64-element (128-byte) swizzled rows.
-bool map_a(CUtensorMap* m, const void* A, int lda, int transA, int M, int K) {
-  if (!transA) return tmap2d(m, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, lda, 64, kTileM,
+bool map_a(CUtensorMap* m, const void* A, int lda, int transA, int M, int K, int box_rows = kTileM) {
+  if (!transA) return tmap2d(m, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, lda, 64, box_rows,
                              CU_TENSOR_MAP_SWIZZLE_128B);
   return tmap2d(m, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, lda, 64, 64,
                 CU_TENSOR_MAP_SWIZZLE_128B);
@@ -193,6 +194,8 @@ void coda_set_timeout_ms(int ms) {
   if (ms < 1) ms = 1;
   g_timeout_ns.store((unsigned long long)ms * 1000000ull);
 }
+
+void coda_set_multicast(int on) { g_multicast.store(on ? 1 : 0); }
 const char* coda_last_error_string(void) { return t_last_error.c_str(); }
 
 coda_status_t coda_get_device_error(coda_stream_t stream) {
@@ -234,7 +237,10 @@ coda_status_t coda_gemm(const void* A, int lda, int transA, const void* B, int l
         "coda_gemm: resid needs transA=0 (and transB=0 for a bf16 output)");
   TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
   PlainArgs a{};
-  CHECK_MAP(map_a(&a.tmA, A, lda, transA, M, K));
+  // the opt-in multicast form covers the plain bf16 GEMM with A K-major and
+  // B MN-major; each CTA then fetches 64-row halves of A
+  a.mc = g_multicast.load() && !transA && !transB && !c_fp32 && !resid && !rowsq_part;
+  CHECK_MAP(map_a(&a.tmA, A, lda, transA, M, K, a.mc ? 64 : kTileM));
   CHECK_MAP(map_b(&a.tmB, B, ldb, transB, N, K));
   if (c_fp32) CHECK_MAP(map_f32_32(&a.tmC, C, M, N, ldc));
   else CHECK_MAP(map_bf16_32(&a.tmC, C, M, N, ldc));

@@ -78,6 +78,14 @@ int coda_row_tiles32(int M);
  * A wait that runs out records CODA_ERR_TIMEOUT and the kernel returns. */
 void coda_set_timeout_ms(int ms);
 
+/* Opt-in TMA multicast (default off): with on != 0, later coda_gemm calls
+ * with a bf16 output, A not transposed, B not transposed and no residual or
+ * row statistic run on clusters of two CTA pairs that compute neighbouring
+ * column tiles of the same rows; each CTA fetches half of the shared A rows
+ * from global memory and multicasts it to its counterpart in the other pair,
+ * halving the L2 reads of A. Single-GPU, own-memory operands only. */
+void coda_set_multicast(int on);
+
 /* Synchronises `stream`, then returns and clears the device error word:
  * CODA_OK, CODA_ERR_TIMEOUT (a bounded wait ran out),
  * CODA_ERR_INVALID_VALUE (a CE target outside [0, V)) or CODA_ERR_RANGE (a
