@@ -63,6 +63,24 @@ def test_ce_bwd_ragged(coda, small_ws):
     assert_close("dW", bw["dW"], ref["dW"], TOL_BF16)
 
 
+def test_ce_bwd_one_row(coda):
+    """One token over the smallest vocabulary (V = 8): one partial tile in
+    every GEMM of the backward."""
+    from gemm_epilogue_fusion_tcgen05_gb300 import blocks
+    sh = LMHeadShape("ce_bwd_one", M=1, d=64, V=8, seed=25)
+    inp = lmhead_inputs(sh)
+    t = inp["targets"]
+    dl = _dloss(sh.M, 1)
+    h, W = inp["hidden"].cuda(), inp["W"].cuda()
+    fw = blocks.lmhead_ce(h, W, t.cuda())
+    bw = blocks.lmhead_ce_bwd(h, W, t.cuda(), fw["lse"], dl.cuda())
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    ref = O.lmhead_ce_bwd(O.to64(inp["hidden"]), O.to64(inp["W"]), t.numpy(), dl.double().numpy())
+    assert_close("dhidden", bw["dhidden"], ref["dhidden"], TOL_BF16)
+    assert_close("dW", bw["dW"], ref["dW"], TOL_BF16)
+
+
 def test_ce_bwd_full_size(coda):
     from gemm_epilogue_fusion_tcgen05_gb300 import blocks
     sh = WORKLOADS["lmhead_ce"]

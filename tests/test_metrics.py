@@ -1,0 +1,40 @@
+"""The error metrics the parity tests use, checked on hand-made values (CPU)."""
+import numpy as np
+import pytest
+
+from tests._util import TOL_F32, assert_close, assert_stat_near_exact, maxrel
+
+
+def test_maxrel_is_max_error_over_max_reference():
+    assert maxrel(np.array([1.0, 2.0]), np.array([1.0, 4.0])) == pytest.approx(0.5)
+    assert maxrel(np.array([0.0]), np.array([0.0])) == 0.0
+
+
+def test_maxrel_rejects_non_finite_output():
+    with pytest.raises(AssertionError):
+        maxrel(np.array([np.nan]), np.array([1.0]))
+
+
+def test_assert_close_bound():
+    assert_close("ok", np.array([1.01]), np.array([1.0]), 2e-2)
+    with pytest.raises(AssertionError):
+        assert_close("bad", np.array([1.03]), np.array([1.0]), 2e-2)
+
+
+def test_stat_single_row_within_storage_rounding():
+    # one heavily cancelling row: the storage-rounded value is 2 % from exact,
+    # the GPU value next to it passes; one further away than that fails
+    exact = np.array([-2.8e-5])
+    rounded = exact * 1.02
+    assert_stat_near_exact("s", rounded * (1 + 1e-6), exact, rounded)
+    with pytest.raises(AssertionError):
+        assert_stat_near_exact("s", exact * 1.05, exact, rounded)
+
+
+def test_stat_many_rows_also_needs_the_exact_bound():
+    # within the storage-rounding allowance but beyond TOL_S_EXACT of max |s|
+    exact = np.array([1.0, -0.5, 0.25])
+    rounded = exact + np.array([0.01, 0.0, 0.0])
+    with pytest.raises(AssertionError):
+        assert_stat_near_exact("s", rounded, exact, rounded)
+    assert_stat_near_exact("s", exact + TOL_F32 * 0.5, exact, exact)
