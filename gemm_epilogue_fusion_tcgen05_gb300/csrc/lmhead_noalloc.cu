@@ -66,6 +66,12 @@ extern "C" size_t coda_lmhead_ce_noalloc_capacity(void) { return kNoAllocScratch
 extern "C" coda_status_t coda_lmhead_ce_noalloc(const void* hidden, const void* W,
                                                 const int32_t* targets, float* lse, float* loss,
                                                 int M, int V, int d, coda_stream_t stream) {
+  // sizes first: an argument error is reported as one on any machine, before
+  // the scratch lookup touches the device
+  if (M <= 0 || V <= 0 || d <= 0) {
+    coda::set_last_error("coda_lmhead_ce_noalloc: M, V and d must be positive");
+    return CODA_ERR_INVALID_VALUE;
+  }
   const size_t need = coda_lmhead_ce_workspace_size(M, V);
   if (need > kNoAllocScratchBytes) {
     char buf[320];

@@ -101,3 +101,59 @@ def test_sources_name_no_closed_copy_call():
         for f in files:
             if f.endswith((".cu", ".cuh", ".h", ".py", ".cpp")):
                 assert not pat.search(open(os.path.join(d, f)).read()), f
+
+
+def _empty_calls(L):
+    """Every compute entry point with M = 0 (no rows); the other sizes valid."""
+    ok = P(0x10000)
+    f = ctypes.c_float(1e-6)
+    return {
+        "coda_gemm_resid_norm_stats": lambda M: L.coda_gemm_resid_norm_stats(
+            ok, ok, ok, ok, ok, ok, ok, M, 64, 64, None),
+        "coda_row_rms": lambda M: L.coda_row_rms(ok, 1, M, 64, f, ok, None),
+        "coda_gemm_rowscale_swiglu": lambda M: L.coda_gemm_rowscale_swiglu(
+            ok, ok, ok, ok, None, M, 64, 64, None),
+        "coda_gemm_rope": lambda M: L.coda_gemm_rope(ok, ok, None, ok, 128, 128, 128, ok, None,
+                                                     M, 256, 64, None),
+        "coda_lmhead_ce": lambda M: L.coda_lmhead_ce(ok, ok, ok, ok, ok, ok, 1 << 20, M, 512, 64,
+                                                     None),
+        "coda_lmhead_ce_noalloc": lambda M: L.coda_lmhead_ce_noalloc(ok, ok, ok, ok, ok, M, 512,
+                                                                     64, None),
+        "coda_lmhead_ce_bwd": lambda M: L.coda_lmhead_ce_bwd(ok, ok, ok, ok, ok, ok, ok, ok,
+                                                             1 << 20, M, 512, 64, None),
+        "coda_gemm_rowscale_swiglu_bwd": lambda M: L.coda_gemm_rowscale_swiglu_bwd(
+            ok, ok, ok, ok, ok, ok, M, 64, 64, None),
+        "coda_row_rms_bwd": lambda M: L.coda_row_rms_bwd(ok, 1, M, 64, ok, None),
+        "coda_gemm_resid_norm_stats_bwd": lambda M: L.coda_gemm_resid_norm_stats_bwd(
+            ok, ok, ok, ok, ok, ok, None, ok, ok, M, 64, 128, None),
+        "coda_gemm_rope_bwd": lambda M: L.coda_gemm_rope_bwd(ok, ok, ok, ok, 128, 128, 128, ok, ok,
+                                                             M, 256, 64, None),
+        "coda_gemm_resid_ln_stats": lambda M: L.coda_gemm_resid_ln_stats(
+            ok, ok, ok, ok, ok, ok, ok, ok, M, 64, 64, None),
+        "coda_row_ln": lambda M: L.coda_row_ln(ok, ok, 1, M, 64, f, ok, ok, None),
+        "coda_gemm_ln_rowscale_swiglu": lambda M: L.coda_gemm_ln_rowscale_swiglu(
+            ok, ok, ok, ok, ok, ok, ok, None, M, 64, 64, None),
+        "coda_gemm_ln_rowscale_swiglu_bwd": lambda M: L.coda_gemm_ln_rowscale_swiglu_bwd(
+            ok, ok, ok, ok, ok, ok, ok, ok, ok, ok, M, 64, 64, None),
+        "coda_row_ln_bwd": lambda M: L.coda_row_ln_bwd(ok, ok, ok, 1, M, 64, ok, ok, None),
+        "coda_gemm_resid_ln_stats_bwd": lambda M: L.coda_gemm_resid_ln_stats_bwd(
+            ok, ok, ok, ok, ok, ok, ok, ok, ok, None, ok, None, ok, ok, M, 64, 128, None),
+    }
+
+
+def test_every_entry_point_rejects_empty_and_negative_rows(L):
+    """No rows (or a negative count) is an argument error on the host for
+    every compute entry point, before any device work."""
+    for name, call in _empty_calls(L).items():
+        for M in (0, -1):
+            assert call(M) == 1, f"{name}(M={M})"
+            assert isinstance(L.coda_last_error_string(), bytes)
+    covered = set(_empty_calls(L))
+    compute = {n for n in declared_symbols()
+               if n not in ("coda_gemm", "coda_col_reduce", "coda_rope_table", "coda_col_tiles",
+                            "coda_row_tiles32", "coda_lmhead_ce_workspace_size",
+                            "coda_lmhead_ce_bwd_workspace_size", "coda_lmhead_ce_noalloc_capacity",
+                            "coda_last_error_string",
+                            "coda_get_device_error", "coda_set_timeout_ms", "coda_set_multicast",
+                            "coda_selftest_bounded_wait", "coda_version")}
+    assert compute <= covered, sorted(compute - covered)
