@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import dataclasses
+import datetime
 import hashlib
 import json
 import os
@@ -65,8 +66,9 @@ def _smi_id(local: int) -> str:
 
 
 class Clocks:
-    """Samples nvidia-smi every 200 ms while the timed region runs."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """Samples nvidia-smi every 50 ms around the timed region; `stop` keeps
+    the samples whose nvidia-smi timestamp falls inside the region."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -79,7 +81,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-i", str(self.idx), "-lms", "200"], stdout=subprocess.PIPE,
+                 "-i", str(self.idx), "-lms", "50"], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -90,7 +92,31 @@ class Clocks:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    @staticmethod
+    def parse(lines, window=None):
+        """Median SM clock, max clock and the throttle reasons seen, from
+        nvidia-smi CSV lines; with window = (t0, t1) (seconds since the
+        epoch) only the samples stamped inside it count, if there are any."""
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
+        for ln in lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if window and window[0] <= r[0] <= window[1]]
+        use = inside or rows
+        sm = sorted(r[1] for r in use)
+        reasons = sorted({n for r in use for n, v in zip(names, r[3]) if v.lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": use[-1][2] if use else None, "reasons": reasons,
+                "samples": len(use), "in_timed_region": bool(inside)}
+
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -99,24 +125,7 @@ class Clocks:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.t.join(timeout=2)
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        sm.sort()
-        med = sm[len(sm) // 2] if sm else None
-        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return self.parse(self.lines, window)
 
 
 def _kernel_hash():
@@ -400,6 +409,7 @@ def run_coda(args):
     clocks.start()
     time.sleep(0.3)
     wall0 = time.perf_counter()
+    t_epoch0 = time.time()
     for i in range(args.steps):
         flush.fill_(float(i))
         step_ev[i][0].record(stream)
@@ -407,9 +417,10 @@ def run_coda(args):
         step_ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    t_epoch1 = time.time()
     if ws > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(window=(t_epoch0, t_epoch1))
     st = C.get_device_error()
     if st != 0:
         raise SystemExit(f"device error in timed region: {st}")
