@@ -959,12 +959,34 @@ def run_primitives(args):
             lambda: C.coda_lmhead_ce(A, B, t, lse, loss, ws),
             lambda: F.cross_entropy((A @ B).float(), t.long(), reduction="none")),
     }
+    # what each fused call produced, to set against the unfused result
+    fused_out = {
+        "pairwise map (SwiGLU)": lambda: half,
+        "row vector (scale r[m])": lambda: out,
+        "tile load (residual)": lambda: out,
+        "tile reduction (row sum of squares)": lambda: part.sum(0),
+        "stateful max/sum-exp (LSE + CE)": lambda: loss,
+    }
+    unfused_out = {"tile reduction (row sum of squares)": lambda u: u[1]}
+
+    def maxrel(a, b):
+        a, b = a.float(), b.float()
+        return float((a - b).abs().max() / b.abs().max().clamp_min(1e-30))
+
     gemm_ms = timeit(lambda: torch.matmul(A, B, out=out))
     res = {}
     for name, (fused, unfused) in cases.items():
         fm, um = timeit(fused), timeit(unfused)
+        fused()
+        got = fused_out[name]().clone()
+        want = unfused_out.get(name, lambda u: u)(unfused())
         res[name] = {"fused_ms": round(fm, 4), "cublas_plus_kernel_ms": round(um, 4),
-                     "speedup": round(um / fm, 3)}
+                     "speedup": round(um / fm, 3),
+                     # the unfused path rounds its GEMM output to bf16 first
+                     "max_rel_diff_vs_unfused": round(maxrel(got, want), 6)}
+    st = C.get_device_error()
+    if st != 0:
+        raise SystemExit(f"device error {st}")
     line = {"metric": "epilogue primitives: fused GEMM+epilogue vs cuBLAS + separate kernel",
             "shape": [M, N, K], "cublas_gemm_alone_ms": round(gemm_ms, 4), "primitives": res}
     print(json.dumps(line), flush=True)
