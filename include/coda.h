@@ -199,9 +199,12 @@ coda_status_t coda_lmhead_ce(const void* hidden, const void* W, const int32_t* t
  * that receives only its inputs and outputs while a host framework's
  * allocator owns the rest of the device, or a loop where cudaMalloc /
  * cudaFree (which can synchronise the device) are not allowed.
- *   - M and V must satisfy coda_lmhead_ce_workspace_size(M, V) <=
- *     coda_lmhead_ce_noalloc_capacity() (about 4100 rows at V = 128256);
- *     larger requests return CODA_ERR_INVALID_VALUE with an explanation.
+ *   - M, V and d must be positive (else CODA_ERR_INVALID_VALUE, before any
+ *     device call), and M and V must satisfy
+ *     coda_lmhead_ce_workspace_size(M, V) <= coda_lmhead_ce_noalloc_capacity()
+ *     (about 4100 rows at V = 128256); larger requests return
+ *     CODA_ERR_INVALID_VALUE with an explanation. The remaining argument
+ *     checks are those of coda_lmhead_ce.
  *   - The first call on each device looks the array's device address up
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
