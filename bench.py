@@ -789,6 +789,8 @@ KERNEL_CASES = {
     # the 1B block's SwiGLU GEMM at half its rows (a bf16 + the fp16 saved y)
     "swiglu_4096x16384x2048": dict(M=4096, N=16384, K=2048, kind="swiglu"),
     "fwd_4096x16384x2048": dict(M=4096, N=16384, K=2048, transA=False, f32=False),
+    # the LM head + CE at a quarter of its tokens (W, 525 MB, still far larger than L2)
+    "lmhead_2048x128256x2048": dict(M=2048, N=128256, K=2048, kind="lmhead"),
 }
 
 
@@ -817,6 +819,14 @@ def run_kernel_case(args):
         out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         save = torch.empty((M, N), dtype=torch.float16, device=dev)
         fn = lambda: C.coda_gemm_rope(A, B, r, table, 4096, 128, N - 1024, out, save)
+    elif cs.get("kind") == "lmhead":
+        A = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
+        B = (torch.randn((K, N), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+        t = torch.randint(0, N, (M,), generator=gen, device=dev, dtype=torch.int32)
+        lse = torch.empty(M, dtype=torch.float32, device=dev)
+        loss = torch.empty(M, dtype=torch.float32, device=dev)
+        ws = torch.empty(C.coda_lmhead_ce_workspace_size(M, N), dtype=torch.uint8, device=dev)
+        fn = lambda: C.coda_lmhead_ce(A, B, t, lse, loss, ws)
     else:
         A = torch.randn((K, M) if cs["transA"] else (M, K), generator=gen, device=dev).to(torch.bfloat16)
         B = torch.randn((K, N), generator=gen, device=dev).to(torch.bfloat16)
