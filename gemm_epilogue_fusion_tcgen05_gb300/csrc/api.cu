@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -22,6 +23,18 @@ thread_local std::string t_last_error;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_multicast{0};
 
+// Every host-side error message lands here; with the environment variable
+// CODA_DEBUG set to anything but "0" (read once) it is also written to
+// stderr as it happens.
+void note_host_error(const char* msg) {
+  t_last_error = msg;
+  static const bool echo = [] {
+    const char* v = std::getenv("CODA_DEBUG");
+    return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+  }();
+  if (echo) std::fprintf(stderr, "libcoda: %s\n", msg);
+}
+
 coda_status_t fail(coda_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 coda_status_t fail(coda_status_t s, const char* fmt, ...) {
   char buf[512];
@@ -29,7 +42,7 @@ coda_status_t fail(coda_status_t s, const char* fmt, ...) {
   va_start(ap, fmt);
   vsnprintf(buf, sizeof(buf), fmt, ap);
   va_end(ap);
-  t_last_error = buf;
+  note_host_error(buf);
   return s;
 }
 
@@ -182,7 +195,7 @@ constexpr int kMaxDim = 1 << 30;
 
 namespace coda {
 // lets other translation units of the library report a host-side error
-void set_last_error(const char* msg) { t_last_error = msg; }
+void set_last_error(const char* msg) { note_host_error(msg); }
 }  // namespace coda
 
 extern "C" {

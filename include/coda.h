@@ -95,7 +95,10 @@ void coda_set_multicast(int on);
  * launch on several streams of one device should read it from one place. */
 coda_status_t coda_get_device_error(coda_stream_t stream);
 
-/* Text of the last error seen by this thread (never NULL). */
+/* Text of the last error seen by this thread (never NULL). With the
+ * environment variable CODA_DEBUG set to anything but "0" when the library
+ * first records an error, every host-side error message is also written to
+ * stderr, prefixed "libcoda: ", as it is recorded. */
 const char* coda_last_error_string(void);
 
 /* ------------------------------------------------------------------ GEMM */

@@ -157,3 +157,28 @@ def test_every_entry_point_rejects_empty_and_negative_rows(L):
                             "coda_get_device_error", "coda_set_timeout_ms", "coda_set_multicast",
                             "coda_selftest_bounded_wait", "coda_version")}
     assert compute <= covered, sorted(compute - covered)
+
+
+def _run_bad_call(env_value):
+    """A child process that makes one call with an argument error."""
+    import subprocess
+    import sys
+    env = dict(os.environ)
+    env.pop("CODA_DEBUG", None)
+    if env_value is not None:
+        env["CODA_DEBUG"] = env_value
+    code = ("import ctypes, gemm_epilogue_fusion_tcgen05_gb300 as c; L = c.lib(); "
+            "ok = ctypes.c_void_p(0x10000); "
+            "print(L.coda_gemm(ok, 64, 0, ok, 64, 0, None, None, ok, 64, 0, 0, 64, 64, None))")
+    return subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                          text=True, timeout=120)
+
+
+def test_coda_debug_echoes_host_errors_to_stderr(L):
+    on = _run_bad_call("1")
+    assert on.returncode == 0 and on.stdout.strip() == "1"
+    assert "libcoda: coda_gemm" in on.stderr
+    for quiet in (None, "0"):
+        off = _run_bad_call(quiet)
+        assert off.returncode == 0 and off.stdout.strip() == "1"
+        assert "libcoda:" not in off.stderr
