@@ -31,9 +31,19 @@ def maxrel(got, ref) -> float:
     return float(np.max(np.abs(got - ref)) / max(float(np.max(np.abs(ref))), 1e-300))
 
 
+def elementwise_rel(got, ref) -> float:
+    """Largest elementwise relative error |gpu - ref| / max(|ref|, floor),
+    with floor = 1e-3 * rms(ref) so that entries near zero do not dominate.
+    Reported beside the max-norm metric; the bounds apply to the latter."""
+    got = to64(got)
+    ref = to64(ref)
+    floor = 1e-3 * max(float(np.sqrt(np.mean(ref * ref))), 1e-300)
+    return float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), floor)))
+
+
 def assert_close(name, got, ref, tol):
     e = maxrel(got, ref)
-    print(f"{name}: max rel err {e:.3e} (tol {tol:g})")
+    print(f"{name}: max rel err {e:.3e} (tol {tol:g}); elementwise {elementwise_rel(got, ref):.3e}")
     assert e <= tol, f"{name}: max rel err {e:.3e} > {tol:g}"
     return e
 

@@ -2,7 +2,7 @@
 import numpy as np
 import pytest
 
-from tests._util import TOL_F32, assert_close, assert_stat_near_exact, maxrel
+from tests._util import TOL_F32, assert_close, assert_stat_near_exact, elementwise_rel, maxrel
 
 
 def test_maxrel_is_max_error_over_max_reference():
@@ -38,3 +38,11 @@ def test_stat_many_rows_also_needs_the_exact_bound():
     with pytest.raises(AssertionError):
         assert_stat_near_exact("s", rounded, exact, rounded)
     assert_stat_near_exact("s", exact + TOL_F32 * 0.5, exact, exact)
+
+
+def test_elementwise_rel_uses_a_floor_near_zero():
+    ref = np.array([1.0, 1e-9])
+    got = np.array([1.001, 2e-9])
+    # the tiny entry is judged against 1e-3 * rms(ref), not against itself
+    assert elementwise_rel(got, ref) == pytest.approx(1e-3, rel=1e-6)
+    assert elementwise_rel(ref, ref) == 0.0
