@@ -82,9 +82,11 @@ coda_status_t launch_ctx(cudaStream_t st, LaunchCtx& lc) {
   DevInfo& di = g_dev[dev];
   if (di.ok < 0) {
     int major = 0, minor = 0, sms = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // a failed query is reported, not cached as an unsupported device
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return from_cuda(e, "cudaDeviceGetAttribute");
     if (major != 10 || minor != 3) {
       di.ok = 0;
       return fail(CODA_ERR_UNSUPPORTED, "libcoda is built for sm_103a; device %d is sm_%d%d", dev,
@@ -220,7 +222,8 @@ coda_status_t coda_get_device_error(coda_stream_t stream) {
   if (e != cudaSuccess) return from_cuda(e, "read device error word");
   if (v == 0) return CODA_OK;
   const int zero = 0;
-  cudaMemcpyToSymbol(g_coda_err, &zero, sizeof(int));
+  e = cudaMemcpyToSymbol(g_coda_err, &zero, sizeof(int));
+  if (e != cudaSuccess) return from_cuda(e, "clear the device error word");
   const int code = v & 0xff, where = v >> 8;
   if (code == kErrTimeout)
     return fail(CODA_ERR_TIMEOUT, "a bounded wait in a kernel ran out (site %d)", where);
