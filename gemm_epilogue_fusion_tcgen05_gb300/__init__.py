@@ -12,7 +12,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "CodaError", "lib", "LIB_PATH", "EXPORTS", "col_tiles", "row_tiles32", "set_timeout_ms", "set_multicast",
+    "CodaError", "lib", "LIB_PATH", "EXPORTS", "col_tiles", "row_tiles32", "set_timeout_ms",
     "get_device_error", "coda_gemm", "coda_gemm_resid_norm_stats", "coda_row_rms",
     "coda_gemm_rowscale_swiglu", "coda_gemm_rope", "coda_rope_table", "coda_lmhead_ce",
     "coda_lmhead_ce_workspace_size", "coda_gemm_rowscale_swiglu_bwd", "coda_row_rms_bwd",
@@ -38,7 +38,6 @@ EXPORTS = {
     "coda_col_tiles": (_I, [_I]),
     "coda_row_tiles32": (_I, [_I]),
     "coda_set_timeout_ms": (None, [_I]),
-    "coda_set_multicast": (None, [_I]),
     "coda_get_device_error": (_I, [_P]),
     "coda_last_error_string": (ctypes.c_char_p, []),
     "coda_gemm": (_I, [_P, _I, _I, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
@@ -134,11 +133,6 @@ def row_tiles32(M: int) -> int:
 
 def set_timeout_ms(ms: int) -> None:
     lib().coda_set_timeout_ms(ms)
-
-
-def set_multicast(on: bool) -> None:
-    """Opt-in TMA multicast for the plain bf16 GEMM (see coda.h)."""
-    lib().coda_set_multicast(int(bool(on)))
 
 
 def get_device_error(stream=None) -> int:

@@ -21,7 +21,6 @@ __device__ int g_coda_err;  // device error word, one per device
 
 thread_local std::string t_last_error;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
-std::atomic<int> g_multicast{0};
 
 // Every host-side error message lands here; with the environment variable
 // CODA_DEBUG set to anything but "0" (read once) it is also written to
@@ -68,7 +67,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct DevInfo {
   int ok = -1;  // -1 unknown, 0 unsupported, 1 supported
   int num_sms = 0;
-  int* err = nullptr;
 };
 std::mutex g_dev_mu;
 DevInfo g_dev[64];
@@ -92,17 +90,19 @@ coda_status_t launch_ctx(cudaStream_t st, LaunchCtx& lc) {
       return fail(CODA_ERR_UNSUPPORTED, "libcoda is built for sm_103a; device %d is sm_%d%d", dev,
                   major, minor);
     }
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_coda_err);
-    if (e != cudaSuccess) return from_cuda(e, "cudaGetSymbolAddress(error word)");
-    di.err = static_cast<int*>(p);
     di.num_sms = sms;
     di.ok = 1;
   }
   if (di.ok == 0) return fail(CODA_ERR_UNSUPPORTED, "device %d is not sm_103", dev);
   if (!encode_fn()) return fail(CODA_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled not available");
+  // The error word's device address is looked up on every call, not kept:
+  // after a cudaDeviceReset the module is loaded again and a kept address
+  // would point at memory the new context does not own.
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_coda_err);
+  if (e != cudaSuccess) return from_cuda(e, "cudaGetSymbolAddress(error word)");
   lc.stream = st;
-  lc.err = di.err;
+  lc.err = static_cast<int*>(p);
   lc.timeout_ns = g_timeout_ns.load();
   lc.num_sms = di.num_sms;
   return CODA_OK;
@@ -127,8 +127,8 @@ bool tmap2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
 }
 
 // Operand maps for the mainloop: 64-element (128-byte) swizzled rows.
-bool map_a(CUtensorMap* m, const void* A, int lda, int transA, int M, int K, int box_rows = kTileM) {
-  if (!transA) return tmap2d(m, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, lda, 64, box_rows,
+bool map_a(CUtensorMap* m, const void* A, int lda, int transA, int M, int K) {
+  if (!transA) return tmap2d(m, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, lda, 64, kTileM,
                              CU_TENSOR_MAP_SWIZZLE_128B);
   return tmap2d(m, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, lda, 64, 64,
                 CU_TENSOR_MAP_SWIZZLE_128B);
@@ -210,7 +210,6 @@ void coda_set_timeout_ms(int ms) {
   g_timeout_ns.store((unsigned long long)ms * 1000000ull);
 }
 
-void coda_set_multicast(int on) { g_multicast.store(on ? 1 : 0); }
 const char* coda_last_error_string(void) { return t_last_error.c_str(); }
 
 coda_status_t coda_get_device_error(coda_stream_t stream) {
@@ -253,10 +252,7 @@ coda_status_t coda_gemm(const void* A, int lda, int transA, const void* B, int l
         "coda_gemm: resid needs transA=0 (and transB=0 for a bf16 output)");
   TRY_CTX(reinterpret_cast<cudaStream_t>(stream), lc);
   PlainArgs a{};
-  // the opt-in multicast form covers the plain bf16 GEMM with A K-major and
-  // B MN-major; each CTA then fetches 64-row halves of A
-  a.mc = g_multicast.load() && !transA && !transB && !c_fp32 && !resid && !rowsq_part;
-  CHECK_MAP(map_a(&a.tmA, A, lda, transA, M, K, a.mc ? 64 : kTileM));
+  CHECK_MAP(map_a(&a.tmA, A, lda, transA, M, K));
   CHECK_MAP(map_b(&a.tmB, B, ldb, transB, N, K));
   if (c_fp32) CHECK_MAP(map_f32_32(&a.tmC, C, M, N, ldc));
   else CHECK_MAP(map_bf16_32(&a.tmC, C, M, N, ldc));

@@ -25,8 +25,6 @@ constexpr int kEpiBars = 8;     // mbarriers per epilogue warp (tile loads)
 struct GemmArgs {
   int M, N, K;
   int tiles_m, tiles_n, num_tiles, num_kb;
-  int tiles_n_out;                // column tiles of the output (tiles_n counts the multicast
-                                  // form's column pairs)
   int group;                      // tiles are ordered in bands of `group` row (or column) blocks
   int along_m;                    // 1: bands of row blocks (row index fastest inside a band)
   int* err;                       // device error word

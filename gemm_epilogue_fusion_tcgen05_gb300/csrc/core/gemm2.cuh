@@ -35,7 +35,7 @@
 
 namespace coda {
 
-template <int BN_, bool A_MN_, bool B_MN_, class Epi_, int MS_ = 1, int MC_ = 1>
+template <int BN_, bool A_MN_, bool B_MN_, class Epi_, int MS_ = 1>
 struct Gemm2Traits {
   static constexpr int BN = BN_;
   static constexpr bool A_MN = A_MN_;
@@ -44,8 +44,6 @@ struct Gemm2Traits {
   static constexpr int MS = MS_;                          // 128-row slabs of A per CTA
   static constexpr int NACC = MS == 1 ? 2 : 1;            // accumulator buffers in TMEM
   static_assert(MS == 1 || MS == 2, "MS");
-  static constexpr int MC = MC_;                          // CTA pairs sharing A (multicast)
-  static_assert(MC == 1 || (MC == 2 && MS == 1), "MC");
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int SLAB_BYTES = kBM * kBK * 2;        // one 128-row slab of A
   static constexpr int A_BYTES = MS * SLAB_BYTES;         // this CTA's 128 * MS rows
@@ -90,19 +88,17 @@ __global__ void __launch_bounds__(T::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t rank = crank & 1u;          // 0 = issues the pair's MMA, 1 = peer
+  const uint32_t rank = cluster_ctarank();  // 0 = issues the pair's MMA, 1 = peer
   const bool leader = rank == 0;
-  const int pip = (int)(crank >> 1);         // pair within the cluster (multicast form)
-  const uint32_t lead = crank & ~1u;         // this pair's even CTA
-  const uint16_t pair_mask = (uint16_t)(3u << (2 * pip));
-  const int pair = blockIdx.x / (2 * T::MC);  // cluster index: one tile (super-tile) at a time
-  const int npairs = gridDim.x / (2 * T::MC);
+  const uint32_t lead = 0;                   // the pair's even CTA
+  const uint16_t pair_mask = 3u;
+  const int pair = blockIdx.x / 2;           // cluster index: one tile at a time
+  const int npairs = gridDim.x / 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), T::MC);  // one MMA commit per pair that reads the stage
+      mbar_init(empty(s), 1);  // the pair's MMA commit frees the stage
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull(i), 1);
@@ -144,7 +140,6 @@ __global__ void __launch_bounds__(T::kThreads, 1)
       for (int t = pair; t < g.num_tiles && ok; t += npairs) {
         int mb, nb;
         tile_coords(g, t, mb, nb);
-        nb = nb * T::MC + pip;
         const int m0 = (mb * 2 + (int)rank) * T::MS * kBM;
         const int n0 = nb * BN + (int)rank * (BN / 2);
         for (int kb = 0; kb < g.num_kb; ++kb) {
@@ -159,15 +154,6 @@ __global__ void __launch_bounds__(T::kThreads, 1)
           const int k0 = kb * kBK;
           // the band's stationary operand stays in L2 (evict_last); the
           // other streams past with the default policy
-          if constexpr (T::MC == 2) {
-            // this CTA fetches half `pip` (64 rows) of the A rows both pairs'
-            // CTAs of rank `rank` use, into the same offset of both
-            const uint16_t mask = (uint16_t)((1u << rank) | (1u << (2 + rank)));
-            if constexpr (!T::A_MN)
-              tma_load_2d_pair_mc(&tmA, a_dst + pip * 8192, fb, k0, m0 + pip * 64, mask);
-            else
-              tma_load_2d_pair_mc(&tmA, a_dst + pip * 8192, fb, m0 + pip * 64, k0, mask);
-          } else {
 #pragma unroll
           for (int i = 0; i < T::MS; ++i) {
             const uint32_t ad = a_dst + i * T::SLAB_BYTES;
@@ -182,7 +168,6 @@ __global__ void __launch_bounds__(T::kThreads, 1)
                 else tma_load_2d_pair(&tmA, ad + j * 8192, fb, mi + j * 64, k0);
               }
             }
-          }
           }
           if constexpr (!T::B_MN) {
             if (!g.along_m) tma_load_2d_pair_hint(&tmB, b_dst, fb, k0, n0, pol_keep);
@@ -243,10 +228,9 @@ __global__ void __launch_bounds__(T::kThreads, 1)
                 mma_bf16_pair(d_tmem + i * BN, ad, bd, T::IDESC, (kb | k) != 0 ? 1u : 0u);
               }
             }
-            // the stage is free for a producer once every pair that reads
-            // it is done: with multicast, the other pair's CTAs write our
-            // A half and we write theirs
-            mma_commit_pair(empty(stage), T::MC == 2 ? (uint16_t)0xF : pair_mask);
+            // the stage is free for both CTAs' producers once these MMAs
+            // have read it
+            mma_commit_pair(empty(stage), pair_mask);
             if (++stage == S) {
               stage = 0;
               phase ^= 1u;
@@ -279,17 +263,15 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     for (int t = pair; t < g.num_tiles; t += npairs, ++li) {
       int mb, nb;
       tile_coords(g, t, mb, nb);
-      nb = nb * T::MC + pip;
-      const bool real = nb < g.tiles_n_out;  // the multicast form's odd last column
       const int m_cta = (mb * 2 + (int)rank) * T::MS * kBM, n0 = nb * BN;
       const int acc = li % T::NACC;
-      if (real) T::Epi::template prefetch<BN>(ep, ctx, g, m_cta, n0);
+      T::Epi::template prefetch<BN>(ep, ctx, g, m_cta, n0);
       bool ok = mbar_wait_cluster(tfull(acc), (li / T::NACC) & 1, e, 24);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int i = 0; i < T::MS && ok && real; ++i) {
+      for (int i = 0; i < T::MS && ok; ++i) {
         const int m0 = m_cta + i * kBM;
         if (i > 0) T::Epi::template prefetch<BN>(ep, ctx, g, m0, n0);
         const uint32_t taddr =

@@ -73,9 +73,8 @@ inline bool prefer_two_slabs(int M, int N, int K, int bn, int pairs, double epi_
   return w2 * (2.0 * kTwoSlabCost + epi_kb / kblocks) < 0.97 * w1;
 }
 
-// Launch of the CTA-pair kernel: clusters of 2 (4 in the multicast form, two
-// pairs per column pair of tiles), grid = cluster size x min(tiles,
-// co-resident clusters).
+// Launch of the CTA-pair kernel: clusters of 2, grid = 2 x min(tiles,
+// co-resident pairs).
 template <class T>
 cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const typename T::Epi::Params& ep, int M, int N, int K, const LaunchCtx& lc) {
@@ -87,7 +86,7 @@ cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2 * T::MC;
+  at[0].val.clusterDim.x = 2;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   // programmatic dependent launch: the kernel's prologue may overlap the
@@ -104,7 +103,7 @@ cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
     e = cudaFuncSetAttribute(gemm2_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              T::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(2 * T::MC, 1, 1);
+    cfg.gridDim = dim3(2, 1, 1);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, gemm2_kernel<T>, &cfg);
     if (e != cudaSuccess) return e;
@@ -118,15 +117,14 @@ cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
   g.K = K;
   constexpr int kPairRows = 2 * T::MS * kBM;
   g.tiles_m = (M + kPairRows - 1) / kPairRows;
-  g.tiles_n_out = (N + T::BN - 1) / T::BN;
-  g.tiles_n = (g.tiles_n_out + T::MC - 1) / T::MC;  // units the clusters walk
+  g.tiles_n = (N + T::BN - 1) / T::BN;
   g.num_tiles = g.tiles_m * g.tiles_n;
   g.num_kb = (K + kBK - 1) / kBK;
   const int pairs = g.num_tiles < pairs_max ? g.num_tiles : pairs_max;  // clusters
-  choose_tile_order(g, kPairRows, T::MC * T::BN, K, pairs);
+  choose_tile_order(g, kPairRows, T::BN, K, pairs);
   g.err = lc.err;
   g.timeout_ns = lc.timeout_ns;
-  cfg.gridDim = dim3(2 * T::MC * pairs, 1, 1);
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, gemm2_kernel<T>, tmA, tmB, ep, g);
   if (e != cudaSuccess) return e;

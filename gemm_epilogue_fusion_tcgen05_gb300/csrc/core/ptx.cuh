@@ -309,19 +309,6 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(const CUtensorMap* m, uint
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
-// Multicast form: the box lands at the same shared offset in every CTA of
-// `mask`; with .cta_group::2 the transaction bytes are counted on the barrier
-// at `bar`'s offset in the even CTA of each destination CTA's pair. `bar` is
-// the cluster address of that barrier in this CTA's own even CTA (the peer
-// bit of the address clear).
-__device__ __forceinline__ void tma_load_2d_pair_mc(const CUtensorMap* m, uint32_t dst,
-                                                    uint32_t bar, int x, int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
                "r"(ncols)

@@ -4,10 +4,10 @@
 
 namespace coda {
 
-template <bool AMN, bool BMN, bool F32, bool R, bool Q, int MS = 1, int MC = 1>
+template <bool AMN, bool BMN, bool F32, bool R, bool Q, int MS = 1>
 static cudaError_t plain_impl(const PlainArgs& a, const LaunchCtx& lc) {
   using E = EpiPlain<F32, R, Q>;
-  using T = Gemm2Traits<kTileN, AMN, BMN, E, MS, MC>;
+  using T = Gemm2Traits<kTileN, AMN, BMN, E, MS>;
   typename E::Params p{};
   p.tm_c = a.tmC;
   p.resid = a.resid_ptr;
@@ -29,8 +29,6 @@ cudaError_t launch_plain(const PlainArgs& a, const LaunchCtx& lc) {
     if (a.resid && a.rowsq) return plain_impl<false, true, false, true, true>(a, lc);
     if (a.resid) return plain_impl<false, true, false, true, false>(a, lc);
     if (a.rowsq) return plain_impl<false, true, false, false, true>(a, lc);
-    // opt-in multicast form (coda_set_multicast): two CTA pairs share A
-    if (a.mc) return plain_impl<false, true, false, false, false, 1, 2>(a, lc);
     return two ? plain_impl<false, true, false, false, false, 2>(a, lc)
                : plain_impl<false, true, false, false, false>(a, lc);
   }

@@ -24,7 +24,6 @@ struct PlainArgs {
   bool a_mn, b_mn, out_f32, resid, rowsq;
   const void* resid_ptr;   // [M, N] with the output's type (read by the epilogue without TMA)
   size_t ld_res;           // its row stride in bytes
-  int mc;                  // 1: the A map has 64-row boxes for the multicast form
   float* rowsq_part;
   int M, N, K;
 };

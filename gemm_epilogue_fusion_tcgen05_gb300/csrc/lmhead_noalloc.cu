@@ -13,10 +13,13 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library keeps kNoAllocScratchBytes of it until the process exits. Host
 // code may not pass the array's name to a kernel (on the host it is only a
-// stand-in symbol); its device address is looked up once per device with
-// cudaGetSymbolAddress, on the first call made while that device is current.
+// stand-in symbol); its device address on the current device is looked up
+// with cudaGetSymbolAddress on every call. Nothing is kept between calls, so
+// a cudaDeviceReset (after which the module is loaded again, possibly at
+// another address) leaves no stale pointer behind. The first call on a
+// device may load the library's module there; make it before any stream
+// capture.
 #include <cstdio>
-#include <mutex>
 
 #include "coda.h"
 #include "internal.h"
@@ -27,35 +30,19 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 
 static __device__ __align__(256) unsigned char g_lmhead_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_ptr[64] = {};
-
-// Device address of g_lmhead_scratch on the current device (looked up once).
+// Device address of g_lmhead_scratch on the current device. The lookup is a
+// host-side query of the loaded module: no allocation, no stream operation.
 coda_status_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    coda::set_last_error(cudaGetErrorString(e));
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_lmhead_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    char buf[256];
+    snprintf(buf, sizeof(buf), "coda_lmhead_ce_noalloc: cudaGetSymbolAddress failed: %s",
+             cudaGetErrorString(e));
+    coda::set_last_error(buf);
     return CODA_ERR_LAUNCH;
   }
-  if (dev < 0 || dev >= 64) {
-    coda::set_last_error("coda_lmhead_ce_noalloc: device index out of range");
-    return CODA_ERR_UNSUPPORTED;
-  }
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_lmhead_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      char buf[256];
-      snprintf(buf, sizeof(buf), "coda_lmhead_ce_noalloc: cudaGetSymbolAddress failed: %s",
-               cudaGetErrorString(e));
-      coda::set_last_error(buf);
-      return CODA_ERR_LAUNCH;
-    }
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return CODA_OK;
 }
 

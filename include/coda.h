@@ -78,14 +78,6 @@ int coda_row_tiles32(int M);
  * A wait that runs out records CODA_ERR_TIMEOUT and the kernel returns. */
 void coda_set_timeout_ms(int ms);
 
-/* Opt-in TMA multicast (default off): with on != 0, later coda_gemm calls
- * with a bf16 output, A not transposed, B not transposed and no residual or
- * row statistic run on clusters of two CTA pairs that compute neighbouring
- * column tiles of the same rows; each CTA fetches half of the shared A rows
- * from global memory and multicasts it to its counterpart in the other pair,
- * halving the L2 reads of A. Single-GPU, own-memory operands only. */
-void coda_set_multicast(int on);
-
 /* Synchronises `stream`, then returns and clears the device error word:
  * CODA_OK, CODA_ERR_TIMEOUT (a bounded wait ran out),
  * CODA_ERR_INVALID_VALUE (a CE target outside [0, V)) or CODA_ERR_RANGE (a
@@ -208,9 +200,11 @@ coda_status_t coda_lmhead_ce(const void* hidden, const void* W, const int32_t* t
  *     (about 4100 rows at V = 128256); larger requests return
  *     CODA_ERR_INVALID_VALUE with an explanation. The remaining argument
  *     checks are those of coda_lmhead_ce.
- *   - The first call on each device looks the array's device address up
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - Every call looks the array's device address up on the current device
+ *     (cudaGetSymbolAddress, a host-side query) and keeps nothing, so the
+ *     call stays valid after a cudaDeviceReset. The first call on a device
+ *     may load the library's module there: make it before any stream
+ *     capture.
  *   - All calls share the array: calls whose work overlaps on the GPU (e.g.
  *     on two streams at once) race and give wrong results. Each call
  *     rewrites every entry it reads, so no clearing is needed.

@@ -154,7 +154,7 @@ def test_every_entry_point_rejects_empty_and_negative_rows(L):
                             "coda_row_tiles32", "coda_lmhead_ce_workspace_size",
                             "coda_lmhead_ce_bwd_workspace_size", "coda_lmhead_ce_noalloc_capacity",
                             "coda_last_error_string",
-                            "coda_get_device_error", "coda_set_timeout_ms", "coda_set_multicast",
+                            "coda_get_device_error", "coda_set_timeout_ms",
                             "coda_selftest_bounded_wait", "coda_version")}
     assert compute <= covered, sorted(compute - covered)
 

@@ -152,31 +152,6 @@ def test_gemm_resid_row_ends_inside_a_vector(coda, c_fp32):
     assert torch.all(Cbig[:, N:] == 0), "wrote outside the logical columns"
 
 
-@pytest.mark.parametrize("MNK", [(1000, 1800, 264), (4096, 4864, 4096), (256, 256, 64), (8192, 7424, 2048)])
-def test_gemm_multicast_form(coda, MNK):
-    """The opt-in multicast form (clusters of two CTA pairs sharing A):
-    ragged M and K, an odd number of 256-column tiles (the last pair of a
-    cluster has no real tile: 1800 -> 8 tiles... 4864 -> 19, 7424 -> 29), and
-    more tiles than clusters. Waits are bounded at 500 ms here."""
-    M, N, K = MNK
-    A, B = _rand((M, K), 31), _rand((K, N), 32, 0.1)
-    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    coda.set_timeout_ms(500)
-    coda.set_multicast(True)
-    try:
-        coda.coda_gemm(A.cuda(), B.cuda(), C)
-        torch.cuda.synchronize()
-        st = coda.get_device_error()
-    finally:
-        coda.set_multicast(False)
-        coda.set_timeout_ms(2000)
-    assert st == 0, f"device status {st}"
-    rng = np.random.default_rng(33)
-    rows = np.array(sorted(set(rng.choice(M, min(M, 64), replace=False).tolist()) | {0, M - 1}))
-    ref = to64(A)[rows] @ to64(B)
-    assert_close(f"multicast gemm {MNK}", C[rows].cpu(), ref, TOL_BF16)
-
-
 def test_bounded_wait_gives_up_without_fault(coda):
     st = coda.coda_selftest_bounded_wait(20)
     assert st == coda.CODA_ERR_TIMEOUT

@@ -176,20 +176,6 @@ def test_layernorm_block_forward_and_backward_outputs(coda):
     _check_all(coda, o)
 
 
-def test_multicast_form_writes_only_its_rows_and_columns(coda):
-    """The opt-in form where two CTA pairs share A (an odd number of column
-    tiles, so one cluster's second pair has no tile)."""
-    N, K = 520, 136  # 3 column tiles (the last one 8 columns wide)
-    A, B = _bf(M, K, seed=25), _bf(K, N, seed=26)
-    C = Guarded((M, N), torch.bfloat16, ld=N + 8)
-    coda.set_multicast(True)
-    try:
-        coda.coda_gemm(A, B, C.t)
-        _check_all(coda, {"C": C})
-    finally:
-        coda.set_multicast(False)
-
-
 def test_noalloc_lmhead_writes_only_its_outputs(coda):
     hid, W = _bf(M, D, seed=27), _bf(D, V, std=0.05, seed=28)
     g = torch.Generator(device="cuda").manual_seed(29)
