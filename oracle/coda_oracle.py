@@ -89,42 +89,81 @@ def _store_saved(store_bf16: bool):
     return f16_round if store_bf16 else (lambda t: t)
 
 
+def tc_matmul(a, b, group: int = 16) -> np.ndarray:
+    """A model of a tensor-core GEMM with an fp32 accumulator, for operands
+    that are exact in fp32 (bf16 / fp16 values): along K, each group of
+    `group` products is summed exactly (in fp64, which holds these sums
+    without rounding for the sizes used here) and added to the fp32
+    accumulator, and that addition rounds toward zero (drops the bits below
+    fp32's 24-bit significand). Truncating accumulation is what the fp32
+    results of a GEMM on this hardware show: their error is biased toward
+    zero and some twenty times a round-to-nearest fp32 GEMM's; this model
+    errs slightly more than the hardware (a GPU test checks both). Returns
+    fp32 values."""
+    a = np.asarray(a, dtype=f64)
+    b = np.asarray(b, dtype=f64)
+    keep = np.uint64(0xFFFFFFFFE0000000)  # sign, exponent, top 23 fraction bits
+    acc = np.zeros((a.shape[0], b.shape[1]), dtype=f64)
+    for k0 in range(0, a.shape[1], group):
+        acc += a[:, k0:k0 + group] @ b[k0:k0 + group, :]
+        acc = (acc.view(np.uint64) & keep).view(f64)
+    return acc.astype(np.float32)
+
+
+def _precision(fp32: bool):
+    """Arithmetic of the rewritten forms: fp64 by default. fp32=True runs the
+    same steps as an fp32 tensor-core implementation would: GEMMs through
+    tc_matmul, elementwise maps and row sums in fp32. It serves only to
+    measure how far that arithmetic by itself moves a result from the fp64
+    one; it is meant for store_bf16=True, where the stored tensors are bf16
+    / fp16 values and so exact in fp32. Returns (dtype, matmul)."""
+    if fp32:
+        return np.float32, tc_matmul
+    return f64, (lambda x, y: x @ y)
+
+
+def _stored(rounder, dt):
+    """A storage point that rounds (bf16 / fp16, or not at all) and hands the
+    value on in the arithmetic type dt."""
+    return lambda t: np.asarray(rounder(t), dtype=dt)
+
+
 # --------------------------------------------------------------------------
 # elementwise maps
 # --------------------------------------------------------------------------
 
-def sigmoid(t):
-    t = np.asarray(t, dtype=f64)
+def sigmoid(t, dtype=f64):
+    t = np.asarray(t, dtype=dtype)
     return 1.0 / (1.0 + np.exp(-t))
 
 
-def silu(t):
+def silu(t, dtype=f64):
     """silu(t) = t * sigmoid(t) (the SwiGLU gate activation)."""
-    t = np.asarray(t, dtype=f64)
-    return t * sigmoid(t)
+    t = np.asarray(t, dtype=dtype)
+    return t * sigmoid(t, dtype)
 
 
-def silu_grad(t):
+def silu_grad(t, dtype=f64):
     """d silu / dt = sigmoid(t) * (1 + t * (1 - sigmoid(t)))."""
-    t = np.asarray(t, dtype=f64)
-    s = sigmoid(t)
+    t = np.asarray(t, dtype=dtype)
+    s = sigmoid(t, dtype)
     return s * (1.0 + t * (1.0 - s))
 
 
-def rms_factor(h, eps: float = EPS):
+def rms_factor(h, eps: float = EPS, dtype=f64):
     """Row-wise inverse RMS: r = 1 / sqrt(mean_j h_j^2 + eps)  [notes s2;
     pith Fig. 5 caption: eps inside the square root]."""
-    h = np.asarray(h, dtype=f64)
+    h = np.asarray(h, dtype=dtype)
     return 1.0 / np.sqrt(np.mean(h * h, axis=1) + eps)
 
 
-def swiglu(y):
+def swiglu(y, dtype=f64):
     """Pairwise SwiGLU on gate/up-interleaved columns: column 2k is gate g_k,
     column 2k+1 is up u_k, output a_k = silu(g_k) * u_k  [pith Fig. 7
     caption; notes s2 "Pairwise activations"]."""
     g = y[:, 0::2]
     u = y[:, 1::2]
-    return silu(g) * u
+    return silu(g, dtype) * u
 
 
 # --------------------------------------------------------------------------
@@ -151,7 +190,7 @@ def mlp_fwd(x, z, W0, W1, W2, gamma, eps: float = EPS) -> Dict[str, np.ndarray]:
 
 
 def mlp_fwd_reparam(x, z, W0, W1, W2, gamma, eps: float = EPS,
-                    store_bf16: bool = False) -> Dict[str, np.ndarray]:
+                    store_bf16: bool = False, fp32: bool = False) -> Dict[str, np.ndarray]:
     """The pages' rewritten forward [notes s2; pith Fig. 4; thread Pattern 1]:
         GEMM 1 epilogue: h = x W0 + z (stored), hg = h * gamma (stored),
                          row statistic from the unscaled h (Listing 2: the
@@ -164,18 +203,20 @@ def mlp_fwd_reparam(x, z, W0, W1, W2, gamma, eps: float = EPS,
     With store_bf16, each tensor the rewritten kernels store in bf16 (h, hg,
     a, out) is rounded to bf16 where it is written; its consumers read the
     rounded value, the statistics are taken before rounding. The saved y is
-    rounded to fp16 (a is computed from the unrounded y)."""
-    st = _store(store_bf16)
-    sv = _store_saved(store_bf16)
-    x, z, W0, W1, W2, gamma = (np.asarray(t, dtype=f64) for t in (x, z, W0, W1, W2, gamma))
-    h_acc = x @ W0 + z
-    r = rms_factor(h_acc, eps)
+    rounded to fp16 (a is computed from the unrounded y). fp32: the same
+    steps in fp32 arithmetic (see _precision)."""
+    dt, mm = _precision(fp32)
+    st = _stored(_store(store_bf16), dt)
+    sv = _stored(_store_saved(store_bf16), dt)
+    x, z, W0, W1, W2, gamma = (np.asarray(t, dtype=dt) for t in (x, z, W0, W1, W2, gamma))
+    h_acc = mm(x, W0) + z
+    r = rms_factor(h_acc, eps, dt)
     h = st(h_acc)
     hg = st(h_acc * gamma[None, :])
-    y_acc = r[:, None] * (hg @ W1)
-    a = st(swiglu(y_acc))
+    y_acc = r[:, None] * mm(hg, W1)
+    a = st(swiglu(y_acc, dt))
     y = sv(y_acc)
-    out = st(a @ W2)
+    out = st(mm(a, W2))
     return {"h": h, "r": r, "hg": hg, "y": y, "a": a, "out": out}
 
 
@@ -213,7 +254,8 @@ def mlp_bwd(fwd: Dict[str, np.ndarray], x, W0, W1, W2, gamma, dout) -> Dict[str,
 
 
 def mlp_bwd_reparam(fwd: Dict[str, np.ndarray], x, W0, W1, W2, gamma, dout,
-                    store_bf16: bool = False, stat_only: bool = False) -> Dict[str, np.ndarray]:
+                    store_bf16: bool = False, stat_only: bool = False,
+                    fp32: bool = False) -> Dict[str, np.ndarray]:
     """The pages' reverse-fused backward [notes s3 "Reverse Fusion" and
     "Eliminating the RMSNorm backward kernel"], on the tensors saved by
     ``mlp_fwd_reparam`` (h, hg, r, y, a):
@@ -225,27 +267,29 @@ def mlp_bwd_reparam(fwd: Dict[str, np.ndarray], x, W0, W1, W2, gamma, dout,
         GEMM (dyhat W1^T) epilogue: P = r dh2;  dh = gamma * P - r^2 s h ;
             dgamma = sum_rows P * h
         dW1 = hg^T dyhat ; dW2 = a^T dout ; dx = dh W0^T ; dW0 = x^T dh
-    ``stat_only`` stops after s (and dy, dyhat)."""
-    st = _store(store_bf16)
-    x, W0, W1, W2, gamma, dout = (np.asarray(t, dtype=f64) for t in (x, W0, W1, W2, gamma, dout))
-    h, hg, r, y, a = (fwd[k] for k in ("h", "hg", "r", "y", "a"))
+    ``stat_only`` stops after s (and dy, dyhat). fp32: the same steps in
+    fp32 arithmetic (see _precision)."""
+    dt, mm = _precision(fp32)
+    st = _stored(_store(store_bf16), dt)
+    x, W0, W1, W2, gamma, dout = (np.asarray(t, dtype=dt) for t in (x, W0, W1, W2, gamma, dout))
+    h, hg, r, y, a = (np.asarray(fwd[k], dtype=dt) for k in ("h", "hg", "r", "y", "a"))
     d = h.shape[1]
-    da = dout @ W2.T
+    da = mm(dout, W2.T)
     g = y[:, 0::2]
     u = y[:, 1::2]
     dy = np.empty_like(y)
-    dy[:, 0::2] = da * u * silu_grad(g)
-    dy[:, 1::2] = da * silu(g)
+    dy[:, 0::2] = da * u * silu_grad(g, dt)
+    dy[:, 1::2] = da * silu(g, dt)
     s = np.sum(dy * y, axis=1) / d
     dyhat = st(r[:, None] * dy)
     if stat_only:
         return {"dy": dy, "dyhat": dyhat, "s": s}
-    P = dyhat @ W1.T
+    P = mm(dyhat, W1.T)
     dh = st(gamma[None, :] * P - (r * r * s)[:, None] * h)
     dgamma = np.sum(P * h, axis=0)
     dW1 = hg.T @ dyhat
     dW2 = a.T @ dout
-    dx = st(dh @ W0.T)
+    dx = st(mm(dh, W0.T))
     dW0 = x.T @ dh
     return {"dy": dy, "dyhat": dyhat, "s": s, "P": P, "dh": dh, "dz": dh, "dx": dx,
             "dW0": dW0, "dW1": dW1, "dW2": dW2, "dgamma": dgamma}
@@ -395,16 +439,17 @@ def rope_cos_sin(pos, head_dim: int, theta: float = ROPE_THETA):
 
 
 def rope_apply(v, pos, n_rope_cols: int, head_dim: int, theta: float = ROPE_THETA,
-               inverse: bool = False) -> np.ndarray:
+               inverse: bool = False, dtype=f64) -> np.ndarray:
     """Rotate each adjacent feature pair (2i, 2i+1) inside every head_dim-wide
     head of the first n_rope_cols columns by angle pos * theta_i (pith Fig. 7:
     RoPE rotates each feature pair and returns two outputs):
         v'_{2i}   = v_{2i} cos - v_{2i+1} sin
         v'_{2i+1} = v_{2i} sin + v_{2i+1} cos
     Columns from n_rope_cols on are returned unchanged. ``inverse`` rotates by
-    the negative angle (the transpose of the rotation)."""
-    v = np.array(v, dtype=f64, copy=True)
-    c, s = rope_cos_sin(pos, head_dim, theta)
+    the negative angle (the transpose of the rotation). dtype: arithmetic
+    type (the cos / sin values are computed in fp64 and rounded to it)."""
+    v = np.array(v, dtype=dtype, copy=True)
+    c, s = (np.asarray(t, dtype=dtype) for t in rope_cos_sin(pos, head_dim, theta))
     if inverse:
         s = -s
     nh = n_rope_cols // head_dim
@@ -573,7 +618,7 @@ def block8b_bwd(fwd, o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres, pos,
 
 def block8b_fwd_reparam(o, z, Wo, W1, W2, gamma2, gamma1, Wqkv, pos, n_rope_cols: int,
                         head_dim: int, theta: float = ROPE_THETA, eps: float = EPS,
-                        store_bf16: bool = False):
+                        store_bf16: bool = False, fp32: bool = False):
     """The pages' rewritten form of ``block8b_fwd`` [notes s2; pith Fig. 4 and
     Fig. 7]: each RMSNorm is split into a GEMM-epilogue statistic on the
     unscaled residual sum and a delayed row scale in the next GEMM's epilogue:
@@ -585,29 +630,32 @@ def block8b_fwd_reparam(o, z, Wo, W1, W2, gamma2, gamma1, Wqkv, pos, n_rope_cols
     a, out, outg, qkv) are rounded where they are written and read back
     rounded; y and the copy of qkv kept for the backward's statistic
     (``qkv_save``) are rounded to fp16 (the bf16 outputs come from the
-    unrounded values)."""
-    st = _store(store_bf16)
-    sv = _store_saved(store_bf16)
-    o, z, Wo, W1, W2, gamma2, gamma1, Wqkv = (np.asarray(t, dtype=f64) for t in
+    unrounded values). fp32: the same steps in fp32 arithmetic (see
+    _precision)."""
+    dt, mm = _precision(fp32)
+    st = _stored(_store(store_bf16), dt)
+    sv = _stored(_store_saved(store_bf16), dt)
+    o, z, Wo, W1, W2, gamma2, gamma1, Wqkv = (np.asarray(t, dtype=dt) for t in
                                                (o, z, Wo, W1, W2, gamma2, gamma1, Wqkv))
-    h_acc = o @ Wo + z
-    r = rms_factor(h_acc, eps)
+    h_acc = mm(o, Wo) + z
+    r = rms_factor(h_acc, eps, dt)
     h = st(h_acc)
     hg = st(h_acc * gamma2[None, :])
-    y = r[:, None] * (hg @ W1)
-    a = st(swiglu(y))
-    out_acc = a @ W2 + h
-    r1 = rms_factor(out_acc, eps)
+    y = r[:, None] * mm(hg, W1)
+    a = st(swiglu(y, dt))
+    out_acc = mm(a, W2) + h
+    r1 = rms_factor(out_acc, eps, dt)
     out = st(out_acc)
     outg = st(out_acc * gamma1[None, :])
-    qkv_acc = rope_apply(r1[:, None] * (outg @ Wqkv), pos, n_rope_cols, head_dim, theta)
+    qkv_acc = rope_apply(r1[:, None] * mm(outg, Wqkv), pos, n_rope_cols, head_dim, theta, dtype=dt)
     return {"h": h, "hg": hg, "r": r, "y": sv(y), "a": a, "out": out, "outg": outg, "r1": r1,
             "qkv": st(qkv_acc), "qkv_save": sv(qkv_acc)}
 
 
 def block8b_bwd_reparam(fwd, o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres, pos,
                         n_rope_cols: int, head_dim: int, theta: float = ROPE_THETA,
-                        store_bf16: bool = False, stat_only: bool = False):
+                        store_bf16: bool = False, stat_only: bool = False,
+                        fp32: bool = False):
     """Reverse-fused backward of ``block8b_fwd_reparam`` [notes s3]:
         dqh = r1 R^T dqkv (stored) ; s1 = (1/d) sumcols(dqkv * qkv_save)
         P1 = dqh Wqkv^T ; dout = gamma1 P1 - r1^2 s1 out + dres (stored)
@@ -616,34 +664,38 @@ def block8b_bwd_reparam(fwd, o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres, po
         dyhat = r dy (stored) ; P = dyhat W1^T
         dh = gamma2 P - r^2 s h + dout (stored) ; dgamma2 = sum_rows P * h
         dW2 = a^T dout ; dW1 = hg^T dyhat ; dWo = o^T dh ; do = dh Wo^T
-    ``stat_only`` stops after s1 and s (and the tensors they need)."""
-    st = _store(store_bf16)
+    ``stat_only`` stops after s1 and s (and the tensors they need). fp32:
+    the same steps in fp32 arithmetic (see _precision)."""
+    dt, mm = _precision(fp32)
+    st = _stored(_store(store_bf16), dt)
     o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres = (
-        np.asarray(t, dtype=f64) for t in (o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres))
+        np.asarray(t, dtype=dt) for t in (o, Wo, W1, W2, gamma2, gamma1, Wqkv, dqkv, dres))
+    fwd = {k: np.asarray(v, dtype=dt) for k, v in fwd.items()}
     d = fwd["h"].shape[1]
     r, r1 = fwd["r"], fwd["r1"]
-    dqh = st(r1[:, None] * rope_apply(dqkv, pos, n_rope_cols, head_dim, theta, inverse=True))
+    dqh = st(r1[:, None] * rope_apply(dqkv, pos, n_rope_cols, head_dim, theta, inverse=True,
+                                      dtype=dt))
     s1 = np.sum(dqkv * fwd["qkv_save"], axis=1) / d
-    P1 = dqh @ Wqkv.T
+    P1 = mm(dqh, Wqkv.T)
     dout = st(gamma1[None, :] * P1 - (r1 * r1 * s1)[:, None] * fwd["out"] + dres)
-    da = dout @ W2.T
+    da = mm(dout, W2.T)
     y = fwd["y"]
     g = y[:, 0::2]
     u = y[:, 1::2]
     dy = np.empty_like(y)
-    dy[:, 0::2] = da * u * silu_grad(g)
-    dy[:, 1::2] = da * silu(g)
+    dy[:, 0::2] = da * u * silu_grad(g, dt)
+    dy[:, 1::2] = da * silu(g, dt)
     s = np.sum(dy * y, axis=1) / d
     dyhat = st(r[:, None] * dy)
     res = {"dqkv_hat": dqh, "s1": s1, "dout": dout, "dy": dy, "s": s, "dyhat": dyhat}
     if stat_only:
         return res
-    P = dyhat @ W1.T
+    P = mm(dyhat, W1.T)
     dh = st(gamma2[None, :] * P - (r * r * s)[:, None] * fwd["h"] + dout)
     res.update({"dgamma1": np.sum(P1 * fwd["out"], axis=0), "dWqkv": fwd["outg"].T @ dqh,
                 "dW2": fwd["a"].T @ dout, "dh": dh, "dz": dh,
                 "dgamma2": np.sum(P * fwd["h"], axis=0), "dW1": fwd["hg"].T @ dyhat,
-                "dWo": o.T @ dh, "do": st(dh @ Wo.T)})
+                "dWo": o.T @ dh, "do": st(mm(dh, Wo.T))})
     return res
 
 

@@ -10,7 +10,12 @@ benchmark times (same entry points, same shapes):
     per-row outputs on sampled rows; weight gradients through the property
     dW v = A^T (G v) for random v (A, G the GPU's own saved operands, which
     the sampled rows check); dgamma through its per-32-row partials.
+  * the same block on one 4096-token sequence at full widths: every weight
+    gradient and both dgamma element by element against the full canonical
+    oracle.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -18,7 +23,8 @@ import torch
 from coda_inputs import (WORKLOADS, BlockShape, mlp_block_inputs, ln_block_inputs, lmhead_inputs,
                          block8b_inputs, positions)
 from oracle import coda_oracle as O
-from tests._util import TOL_BF16, TOL_F32, TOL_S_EXACT, assert_close, to64
+from tests._util import (TOL_BF16, TOL_F32, assert_close, assert_stat_near_exact,
+                         chained_stat_tol, rows_8b_full, sampled_rows, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -31,12 +37,6 @@ def coda():
     return c
 
 
-def _rows(M, n=48, seed=0):
-    rng = np.random.default_rng(seed)
-    r = set(rng.choice(M, n, replace=False).tolist()) | {0, 1, 127, 128, M - 1}
-    return np.array(sorted(r))
-
-
 def test_llama1b_forward_sampled_rows(coda):
     from gemm_epilogue_fusion_tcgen05_gb300 import blocks
     sh = WORKLOADS["llama1b_mlp_fwd"]
@@ -45,7 +45,7 @@ def test_llama1b_forward_sampled_rows(coda):
     fw = blocks.mlp_block_fwd(g["x"], g["z"], g["W0"], g["W1"], g["W2"], g["gamma"])
     torch.cuda.synchronize()
     assert coda.get_device_error() == 0
-    rows = _rows(sh.M)
+    rows = sampled_rows(sh.M)
     n = {k: O.to64(v) for k, v in inp.items()}
     ref = O.mlp_fwd(n["x"][rows], n["z"][rows], n["W0"], n["W1"], n["W2"], n["gamma"])
     hg_ref = ref["h"] * n["gamma"][None, :]
@@ -62,7 +62,7 @@ def test_lmhead_ce_full_size_sampled_rows(coda):
     res = blocks.lmhead_ce(inp["hidden"].cuda(), inp["W"].cuda(), inp["targets"].cuda())
     torch.cuda.synchronize()
     assert coda.get_device_error() == 0
-    rows = _rows(sh.M, 40, 1)
+    rows = sampled_rows(sh.M, 40, 1)
     ref = O.lmhead_ce(O.to64(inp["hidden"][rows]), O.to64(inp["W"]), inp["targets"][rows].numpy())
     assert_close("lse", res["lse"].cpu()[rows], ref["lse"], TOL_F32)
     assert_close("loss", res["loss"].cpu()[rows], ref["loss"], TOL_F32)
@@ -87,12 +87,14 @@ def test_llama1b_backward_full_oracle(coda):
     rb = O.mlp_bwd(ref, n["x"], n["W0"], n["W1"], n["W2"], n["gamma"], n["dout"])
     for k in ("dx", "dz", "dW0", "dW1", "dW2", "dgamma"):
         assert_close(k, bw[k], rb[k], TOL_BF16)
-    assert_close("s (exact oracle)", bw["s"], rb["s"], TOL_S_EXACT)
+    s_exact = rb["s"]
     del ref, rb
     st = O.mlp_fwd_reparam(n["x"], n["z"], n["W0"], n["W1"], n["W2"], n["gamma"], store_bf16=True)
     sb = O.mlp_bwd_reparam(st, n["x"], n["W0"], n["W1"], n["W2"], n["gamma"], n["dout"],
                            store_bf16=True, stat_only=True)
-    assert_close("s (storage-rounded oracle)", bw["s"], sb["s"], TOL_F32)
+    tol = chained_stat_tol("llama1b_mlp_bwd", "s")
+    assert_close("s (storage-rounded oracle)", bw["s"], sb["s"], tol)
+    assert_stat_near_exact("s (exact oracle)", bw["s"], s_exact, sb["s"], tol)
 
 
 def test_llama1b_layernorm_block_full_oracle(coda):
@@ -119,14 +121,15 @@ def test_llama1b_layernorm_block_full_oracle(coda):
     rb = O.ln_mlp_bwd(ref, n["x"], n["W0"], n["W1"], n["W2"], n["gamma"], n["beta"], n["dout"])
     for k in ("dx", "dz", "dW0", "dW1", "dW2", "dgamma", "dbeta"):
         assert_close(k, bw[k], rb[k], TOL_BF16)
-    assert_close("s_a (exact oracle)", bw["sa"], rb["sa"], TOL_S_EXACT)
-    assert_close("s_b (exact oracle)", bw["sb"], rb["sb"], TOL_S_EXACT)
+    sa_exact, sb_exact = rb["sa"], rb["sb"]
     del ref, rb
     st = O.ln_mlp_fwd_reparam(*args, store_bf16=True)
     sb = O.ln_mlp_bwd_reparam(st, n["x"], n["W0"], n["W1"], n["W2"], n["gamma"], n["beta"],
                               n["dout"], store_bf16=True)
     assert_close("s_a (storage-rounded oracle)", bw["sa"], sb["sa"], TOL_F32)
     assert_close("s_b (storage-rounded oracle)", bw["sb"], sb["sb"], TOL_F32)
+    assert_stat_near_exact("s_a (exact oracle)", bw["sa"], sa_exact, sb["sa"])
+    assert_stat_near_exact("s_b (exact oracle)", bw["sb"], sb_exact, sb["sb"])
 
 
 def _proj_check(name, dW, A, G, seed):
@@ -155,8 +158,7 @@ def test_llama8b_block_full_size(coda):
     torch.cuda.synchronize()
     assert coda.get_device_error() == 0
     # two whole 32-row blocks (for the dgamma partials) plus scattered rows
-    blk = np.concatenate([np.arange(0, 32), np.arange(sh.M - 32, sh.M)])
-    rows = np.array(sorted(set(blk.tolist()) | set(_rows(sh.M, 16, 2).tolist())))
+    rows = rows_8b_full(sh.M)
     n = {k: O.to64(v[rows]) if v.dim() == 2 and v.shape[0] == sh.M else O.to64(v)
          for k, v in inp.items()}
     pos = positions(sh.M, sh.seq_len).numpy()[rows]
@@ -171,20 +173,21 @@ def test_llama8b_block_full_size(coda):
         assert_close(k, fw[k][ri], want, tol)
     for k in ("dout", "dz", "do"):
         assert_close(k, bw[k][ri], rb[k], TOL_BF16)
-    assert_close("s1 (exact oracle)", bw["s1"][ri], rb["s1"], TOL_S_EXACT)
-    assert_close("s (exact oracle)", bw["s"][ri], rb["s"], TOL_S_EXACT)
     fr = O.block8b_fwd_reparam(n["o"], n["z"], n["Wo"], n["W1"], n["W2"], n["gamma2"], n["gamma1"],
                                n["Wqkv"], pos, sh.n_rope_cols, sh.head_dim, sh.theta, store_bf16=True)
     br = O.block8b_bwd_reparam(fr, n["o"], n["Wo"], n["W1"], n["W2"], n["gamma2"], n["gamma1"],
                                n["Wqkv"], n["dqkv"], n["dres"], pos, sh.n_rope_cols, sh.head_dim,
                                sh.theta, store_bf16=True, stat_only=True)
     # s' and s sit at the end of long bf16 storage cascades (h, hg, a, out,
-    # outg forward; dqkv_hat, dout backward): fp32-vs-fp64 accumulation
-    # differences flip bf16 roundings along them, so the chained values carry
-    # the exact-oracle bound; the kernels' own arithmetic is pinned at 1e-3 in
-    # test_gpu_stages.py
-    assert_close("s1 (storage-rounded oracle)", bw["s1"][ri], br["s1"], TOL_S_EXACT)
-    assert_close("s (storage-rounded oracle)", bw["s"][ri], br["s"], TOL_S_EXACT)
+    # outg forward; dqkv_hat, dout backward): where fp32 tensor-core and fp64
+    # arithmetic round a stored tensor to different bf16 neighbours they
+    # move; the bound is derived from how far the oracle itself moves when it
+    # runs in the tensor-core model's fp32 (tests/golden/stat_spread.json).
+    # The kernels' own arithmetic is pinned at 1e-3 in test_gpu_stages.py.
+    for k in ("s1", "s"):
+        tol = chained_stat_tol("llama8b_block", k)
+        assert_close(f"{k} (storage-rounded oracle)", bw[k][ri], br[k], tol)
+        assert_stat_near_exact(f"{k} (exact oracle)", bw[k][ri], rb[k], br[k], tol)
     # dgamma: the column reduction of its per-32-row partials, and the
     # partials of the two sampled 32-row blocks against the oracle
     for k in ("1", "2"):
@@ -206,3 +209,29 @@ def test_llama8b_block_full_size(coda):
     _proj_check("dW2", bw["dW2"], fw["a"], bw["dout"], 2)
     _proj_check("dW1", bw["dW1"], fw["hg"], bw["dyhat"], 3)
     _proj_check("dWo", bw["dWo"], g["o"], bw["dh"], 4)
+
+
+def test_llama8b_one_sequence_weight_gradients_full_oracle(coda):
+    """One 4096-token sequence of the Llama-3-8B-shaped block (d = 4096,
+    f = 14336, QKV 6144, RoPE theta 5e5): dWo, dW1, dW2, dWqkv, dgamma1 and
+    dgamma2 element by element against the full fp64 canonical oracle."""
+    from gemm_epilogue_fusion_tcgen05_gb300 import blocks
+    sh = dataclasses.replace(WORKLOADS["llama8b_block"], M=4096)
+    inp = block8b_inputs(sh)
+    g = {k: v.cuda() for k, v in inp.items()}
+    cs = blocks.rope_table(sh.seq_len, sh.head_dim, sh.theta, "cuda")
+    fw = blocks.block8b_fwd(g, sh.seq_len, sh.head_dim, sh.n_rope_cols, cs)
+    bw = blocks.block8b_bwd(fw, g, sh.seq_len, sh.head_dim, sh.n_rope_cols, cs)
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    got = {k: to64(bw[k]) for k in ("dWo", "dW1", "dW2", "dWqkv", "dgamma1", "dgamma2")}
+    del fw, bw, g
+    torch.cuda.empty_cache()
+    n = {k: O.to64(v) for k, v in inp.items()}
+    pos = positions(sh.M, sh.seq_len).numpy()
+    ref = O.block8b_fwd(n["o"], n["z"], n["Wo"], n["W1"], n["W2"], n["gamma2"], n["gamma1"],
+                        n["Wqkv"], pos, sh.n_rope_cols, sh.head_dim, sh.theta)
+    rb = O.block8b_bwd(ref, n["o"], n["Wo"], n["W1"], n["W2"], n["gamma2"], n["gamma1"],
+                       n["Wqkv"], n["dqkv"], n["dres"], pos, sh.n_rope_cols, sh.head_dim, sh.theta)
+    for k in ("dWo", "dW1", "dW2", "dWqkv", "dgamma1", "dgamma2"):
+        assert_close(f"{k} (one 4096-token sequence)", got[k], rb[k], TOL_BF16)

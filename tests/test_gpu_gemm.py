@@ -152,6 +152,38 @@ def test_gemm_resid_row_ends_inside_a_vector(coda, c_fp32):
     assert torch.all(Cbig[:, N:] == 0), "wrote outside the logical columns"
 
 
+@pytest.mark.parametrize("MNK,scale_b", [((256, 256, 4096), 0.02), ((256, 512, 2048), 1.0)])
+def test_fp32_accumulation_matches_the_tensor_core_model(coda, MNK, scale_b):
+    """The oracle's fp32 mode models the tensor-core GEMM as 16-product
+    groups added to an fp32 accumulator with truncation (tc_matmul); the
+    bounds on the chained statistics s and s' are derived from it. The
+    kernel's fp32 output must sit closer to that model than to the exact
+    product, err in the same direction (toward zero), and err no more than
+    the model does, so that the model is a conservative stand-in."""
+    from oracle import coda_oracle as O
+    M, N, K = MNK
+    A, B = _rand((M, K), 51), _rand((K, N), 52, scale_b)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    coda.coda_gemm(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    gpu = to64(C)
+    a, b = to64(A), to64(B)
+    exact = a @ b
+    model = O.tc_matmul(a, b).astype(np.float64)
+    scale = np.max(np.abs(exact))
+    e_gpu = np.max(np.abs(gpu - exact)) / scale
+    e_model = np.max(np.abs(model - exact)) / scale
+    d_gm = np.max(np.abs(gpu - model)) / scale
+    bias_gpu = np.mean((gpu - exact) * np.sign(exact)) / np.mean(np.abs(exact))
+    bias_model = np.mean((model - exact) * np.sign(exact)) / np.mean(np.abs(exact))
+    print(f"fp32 GEMM {MNK}: gpu-exact {e_gpu:.2e} model-exact {e_model:.2e} gpu-model {d_gm:.2e}; "
+          f"bias gpu {bias_gpu:.2e} model {bias_model:.2e}")
+    assert d_gm < 0.5 * e_gpu
+    assert bias_gpu < 0 and bias_model < 0
+    assert e_gpu <= e_model and abs(bias_gpu) <= abs(bias_model)
+
+
 def test_bounded_wait_gives_up_without_fault(coda):
     st = coda.coda_selftest_bounded_wait(20)
     assert st == coda.CODA_ERR_TIMEOUT

@@ -31,13 +31,15 @@ def test_stat_single_row_within_storage_rounding():
         assert_stat_near_exact("s", exact * 1.05, exact, rounded)
 
 
-def test_stat_many_rows_also_needs_the_exact_bound():
-    # within the storage-rounding allowance but beyond TOL_S_EXACT of max |s|
+def test_stat_allowance_is_the_given_tolerance():
+    # within the storage-rounding allowance plus tol of max |s| passes; a
+    # value that much further away fails, and a wider tol admits it
     exact = np.array([1.0, -0.5, 0.25])
     rounded = exact + np.array([0.01, 0.0, 0.0])
+    assert_stat_near_exact("s", rounded + TOL_F32 * 0.5, exact, rounded)
     with pytest.raises(AssertionError):
-        assert_stat_near_exact("s", rounded, exact, rounded)
-    assert_stat_near_exact("s", exact + TOL_F32 * 0.5, exact, exact)
+        assert_stat_near_exact("s", rounded + TOL_F32 * 1.5, exact, rounded)
+    assert_stat_near_exact("s", rounded + TOL_F32 * 1.5, exact, rounded, tol=2 * TOL_F32)
 
 
 def test_elementwise_rel_uses_a_floor_near_zero():

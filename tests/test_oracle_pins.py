@@ -616,3 +616,64 @@ def test_planted_mistakes_are_caught(monkeypatch):
         fw = O.mlp_fwd(x, np.array([g["inputs"]["z"]]), np.eye(2), np.eye(2),
                        np.array([[2.0, -1.0]]), np.array([1.0, 0.5]))
         assert abs(fw["r"][0] - g["r"]) > 1e-9
+
+
+# ---------------------------------------------------------------- tensor-core GEMM model
+
+U = 2.0 ** -23  # fp32 spacing just above 1
+
+
+def test_tc_matmul_exact_when_nothing_rounds():
+    # small integers: every group sum and every accumulator value is exact in fp32
+    rng = np.random.default_rng(3)
+    A = rng.integers(-8, 9, (5, 64)).astype(np.float64)
+    B = rng.integers(-8, 9, (64, 7)).astype(np.float64)
+    out = O.tc_matmul(A, B)
+    assert out.dtype == np.float32
+    assert np.array_equal(out.astype(np.float64), A @ B)
+
+
+def test_tc_matmul_truncates_once_per_group_of_16():
+    # row [1, 2^-25 x 31] times ones, K = 32. Group 1 sums exactly to
+    # 1 + 15 * 2^-25 = 1 + 3.75 u and the accumulator keeps 1 + 3 u (toward
+    # zero); group 2 adds 16 * 2^-25 = 4 u exactly: 1 + 7 u. Rounding to
+    # nearest would give 1 + 8 u; truncating every product would give 1.
+    a = np.full((1, 32), 2.0 ** -25)
+    a[0, 0] = 1.0
+    b = np.ones((32, 1))
+    assert float(O.tc_matmul(a, b)[0, 0]) == 1.0 + 7 * U
+    assert float(O.tc_matmul(-a, b)[0, 0]) == -(1.0 + 7 * U)  # toward zero on both sides
+    # with one group of 32 the sum 1 + 7.75 u is truncated once: 1 + 7 u too,
+    # while groups of 1 truncate every 2^-25 away
+    assert float(O.tc_matmul(a, b, group=32)[0, 0]) == 1.0 + 7 * U
+    assert float(O.tc_matmul(a, b, group=1)[0, 0]) == 1.0
+
+
+def test_tc_matmul_error_is_within_the_truncation_bound_and_biased_to_zero():
+    # K/16 truncating additions each lose less than one fp32 ulp of the
+    # running sum, always toward zero
+    rng = np.random.default_rng(4)
+    A = O.bf16_round(rng.standard_normal((64, 2048)))
+    B = O.bf16_round(rng.standard_normal((2048, 48)) * 0.02)
+    exact = A @ B
+    got = O.tc_matmul(A, B).astype(np.float64)
+    # |partial sums| <= sum_k |a_k b_k|: a bound on every running value
+    absmax = np.abs(A) @ np.abs(B)
+    ulp = absmax * 2.0 ** -23
+    assert np.all(np.abs(got - exact) <= (2048 / 16) * ulp)
+    assert np.mean((got - exact) * np.sign(exact)) < 0  # biased toward zero
+    assert rel(got, exact) > 10 * rel((A.astype(np.float32) @ B.astype(np.float32)), exact)
+
+
+def test_fp32_mode_of_the_rewritten_block_is_fp32_and_close():
+    # the fp32 mode runs the same steps; on a small block it agrees with the
+    # fp64 mode to fp32-level error (nothing is stored in bf16 here)
+    b = rand_block(M=4, d=32, f=32, seed=5)
+    args = (b["x"], b["z"], b["W0"], b["W1"], b["W2"], b["gamma"])
+    f64 = O.mlp_fwd_reparam(*args)
+    f32 = O.mlp_fwd_reparam(*args, fp32=True)
+    assert f32["out"].dtype == np.float32 and f32["r"].dtype == np.float32
+    assert rel(f32["out"], f64["out"]) < 1e-5
+    g64 = O.mlp_bwd_reparam(f64, b["x"], b["W0"], b["W1"], b["W2"], b["gamma"], b["dout"])
+    g32 = O.mlp_bwd_reparam(f32, b["x"], b["W0"], b["W1"], b["W2"], b["gamma"], b["dout"], fp32=True)
+    assert rel(g32["s"], g64["s"]) < 1e-4 and rel(g32["dx"], g64["dx"]) < 1e-5

@@ -10,11 +10,13 @@ failure has run every other test before this one.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 from coda_inputs import LMHeadShape, lmhead_inputs
-from tests._util import TOL_F32, assert_close
+from oracle import coda_oracle as O
+from tests._util import TOL_F32, assert_close, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -71,6 +73,14 @@ def test_no_alloc_matches_workspace_entry_point_twice_in_a_row(coda):
         assert coda.get_device_error() == 0
         assert_close(f"lse no-alloc vs workspace ({sh.name})", lse, lse_ref, TOL_F32)
         assert_close(f"loss no-alloc vs workspace ({sh.name})", loss, loss_ref, TOL_F32)
+        # and against the fp64 oracle on sampled rows (first, last, scattered)
+        rng = np.random.default_rng(sh.seed)
+        rows = np.array(sorted({0, sh.M - 1} | set(rng.choice(sh.M, 24, replace=False).tolist())))
+        ref = O.lmhead_ce(to64(inp["hidden"][rows]), to64(inp["W"]),
+                          inp["targets"][rows].cpu().numpy())
+        ri = torch.from_numpy(rows).cuda()
+        assert_close(f"lse no-alloc vs oracle ({sh.name})", lse[ri], ref["lse"], TOL_F32)
+        assert_close(f"loss no-alloc vs oracle ({sh.name})", loss[ri], ref["loss"], TOL_F32)
 
 
 def test_no_alloc_rejects_requests_beyond_its_array(coda):
