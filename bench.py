@@ -1,5 +1,6 @@
 """Benchmark of the CODA GEMM-plus-epilogue hot path on one GB300 (or N
-replicas, one per GPU, under torchrun).
+replicas, one process per GPU: started by torchrun, or by this script itself
+when --gpus N > 1 runs without it).
 
 One step = one pass over every kernel of the hot path:
   * Llama-3-1B-shaped MLP block forward, M=8192, d=2048, f=8192
@@ -449,25 +450,34 @@ def run_coda(args):
     attr_ms = sum(a.elapsed_time(b) for a, b in attr_ev) / n_attr
 
     # end-to-end through the public API with host buffers: copy this step's
-    # inputs host -> device from pinned memory, run, read the results back
+    # inputs host -> device from pinned memory, run, read the results back.
+    # Run right after the timed region, for the same number of steps and
+    # with its own clock record, so that both legs see the same power state.
     ins, outs = step.host_io()
     h_groups = [[t.cpu().pin_memory() for t in group] for group, _ in step.input_groups()]
     h_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for g in h_groups for t in g)
     d2h = sum(t.numel() * t.element_size() for t in h_outs)
-    e2e_steps = 0 if args.only else max(2, min(args.steps, 5))
+    e2e_steps = 0 if args.only else args.steps
     copy_stream = torch.cuda.Stream(device=dev)
+    step.run_from_host(h_groups, h_outs, copy_stream)  # untimed: first use of the copy stream
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_ms = 0.0
+    e2e_ms_list = []
+    clocks_e2e = Clocks(_smi_id(local))
+    clocks_e2e.start()
+    time.sleep(0.3)
+    te0 = time.time()
     for i in range(e2e_steps):
         flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         step.run_from_host(h_groups, h_outs, copy_stream)
         e1.record(stream)
         e1.synchronize()
-        e2e_ms += e0.elapsed_time(e1)
-    e2e_ms /= max(e2e_steps, 1)
+        e2e_ms_list.append(e0.elapsed_time(e1))
+    te1 = time.time()
+    clk_e2e = clocks_e2e.stop(window=(te0, te1)) if e2e_steps else None
+    e2e_ms = sum(e2e_ms_list) / len(e2e_ms_list) if e2e_ms_list else 0.0
     e2e_value = job_throughput(step.flops, ws, max_over_ranks(e2e_ms, dev)) if e2e_ms > 0 else None
 
     peaks, src = _peaks()
@@ -514,10 +524,16 @@ def run_coda(args):
                      "flops_per_launch": fl, "ms_per_launch": round(per_call[k_dom], 4),
                      "traffic": traffic},
         "e2e": {"value": round(e2e_value, 2) if e2e_value else None, "unit": UNIT,
-                "ms_per_step": round(e2e_ms, 4),
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "step_ms": [round(t, 3) for t in e2e_ms_list],
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "per input group on a copy stream; compute waits for a group "
-                          "only before its first reader"},
+                "copies": "each step's activations, upstream gradients and targets copied "
+                          "host -> device from pinned memory per input group on a copy stream "
+                          "(compute waits for a group only before its first reader); the "
+                          "weights stay resident on the device and are not copied; the "
+                          "losses and dgamma are read back",
+                "timing": "the same number of steps as the timed region, run right after it",
+                "clocks": clk_e2e},
         "clocks": clk,
         "step_ms_spread": {"min": round(min(step_ms), 4), "median": round(sorted(step_ms)[len(step_ms) // 2], 4),
                            "max": round(max(step_ms), 4), "all": [round(t, 3) for t in step_ms]},
@@ -535,6 +551,15 @@ def run_coda(args):
         line["graph"] = graph_step(step, flush, args.steps, stream)
     if not args.only and not args.no_next_rows:
         line["next_rows"] = next_rows(step, flush)
+    if not args.only and not args.no_primitives:
+        clk_p = Clocks(_smi_id(local))
+        clk_p.start()
+        time.sleep(0.2)
+        tp0 = time.time()
+        prim = primitives_table(C, dev, reps=5)
+        tp1 = time.time()
+        prim["clocks"] = clk_p.stop(window=(tp0, tp1))
+        line["primitives"] = prim
     if not args.only and not args.no_unfused:
         ref_ms = unfused_reference(step, flush)
         line["unfused_reference"] = {
@@ -905,7 +930,7 @@ def run_profile_pass(args):
 
 # ------------------------------------------------------------------ primitive microbenchmarks
 
-def run_primitives(args):
+def primitives_table(C, dev, reps=7):
     """One GEMM shape (8192 x 8192 x 4096, bf16) with one epilogue primitive
     of each class ("Reading notes on CODA", s1; the pages' Fig. 8 measures
     the same kind of table on H100), fused here vs cuBLAS followed by a
@@ -914,12 +939,8 @@ def run_primitives(args):
       row/column vector load     row scale r[m] (delayed RMSNorm factor)
       tile load/store            residual add
       tile reduction             per-row sum of squares
-      stateful transform         running max / sum-exp (LSE + CE, V = N)"""
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    import __graft_entry__ as g
-    g.build()
-    import gemm_epilogue_fusion_tcgen05_gb300 as C
+      stateful transform         running max / sum-exp (LSE + CE, V = N)
+    Medians of `reps` runs, L2 flushed before each."""
     import torch.nn.functional as F
     gen = torch.Generator(device=dev).manual_seed(7)
     M, N, K = 8192, 8192, 4096
@@ -938,7 +959,7 @@ def run_primitives(args):
     ws = torch.empty(C.coda_lmhead_ce_workspace_size(M, N), dtype=torch.uint8, device=dev)
     flush = torch.empty(128 * 1024 * 1024, dtype=f32, device=dev)
 
-    def timeit(fn, reps=7):
+    def timeit(fn):
         fn()
         torch.cuda.synchronize()
         ts = []
@@ -997,8 +1018,25 @@ def run_primitives(args):
     st = C.get_device_error()
     if st != 0:
         raise SystemExit(f"device error {st}")
+    return {"shape": [M, N, K], "cublas_gemm_alone_ms": round(gemm_ms, 4), "reps": reps,
+            "primitives": res}
+
+
+def run_primitives(args):
+    """The primitive table alone, as its own JSON line."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__ as g
+    g.build()
+    import gemm_epilogue_fusion_tcgen05_gb300 as C
+    clk = Clocks(_smi_id(0))
+    clk.start()
+    time.sleep(0.2)
+    t0 = time.time()
+    tab = primitives_table(C, dev)
+    t1 = time.time()
     line = {"metric": "epilogue primitives: fused GEMM+epilogue vs cuBLAS + separate kernel",
-            "shape": [M, N, K], "cublas_gemm_alone_ms": round(gemm_ms, 4), "primitives": res}
+            **tab, "clocks": clk.stop(window=(t0, t1))}
     print(json.dumps(line), flush=True)
 
 
@@ -1083,9 +1121,80 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def main():
+def launch_ranks(n, argv, timeout_s=3600):
+    """Start n ranks of this script on this node, one process per GPU, the way
+    torchrun does: RANK = LOCAL_RANK = i, WORLD_SIZE = n, rendezvous on
+    127.0.0.1. Each rank is a replica (the path needs no exchange); rank 0
+    prints the line. Returns the worst exit code; if any rank fails, the
+    others are stopped."""
+    port = _free_port()
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__), *argv], env=env))
+    rc = 0
+    t0 = time.time()
+    pending = list(procs)
+    while pending:
+        for p in list(pending):
+            c = p.poll()
+            if c is None:
+                continue
+            pending.remove(p)
+            rc = max(rc, abs(c))
+            if c != 0:
+                for q in pending:
+                    q.terminate()
+        if time.time() - t0 > timeout_s:
+            for q in pending:
+                q.kill()
+            rc = max(rc, 124)
+            break
+        time.sleep(0.1)
+    for p in procs:
+        p.wait()
+    return rc
+
+
+def _free_port():
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def run_probe_ranks(args):
+    """The rank plumbing alone (no GPU work): every rank joins the process
+    group, reports its rank and the device it would use (LOCAL_RANK), and
+    rank 0 prints them. With --backend gloo it runs on CPU."""
+    import torch.distributed as dist
+    ws, rank, local = _dist()
+    backend = args.backend or ("nccl" if torch.cuda.is_available() else "gloo")
+    if ws > 1:
+        dist.init_process_group(backend)
+    me = {"rank": rank, "local_rank": local, "device_index": local, "pid": os.getpid()}
+    allr = [None] * ws
+    if ws > 1:
+        dist.all_gather_object(allr, me)
+        dist.barrier()
+    else:
+        allr = [me]
+    if rank == 0:
+        print(json.dumps({"probe": "ranks", "n_gpus": ws, "backend": backend if ws > 1 else None,
+                          "ranks": allr}), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs (ranks) on this node; under torchrun it must equal WORLD_SIZE, "
+                         "without it N > 1 starts the N ranks itself")
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["coda", "reference"], default="coda")
@@ -1105,11 +1214,26 @@ def main():
                     help="skip the unfused PyTorch reference sequence")
     ap.add_argument("--only", default="", help="time only these calls (comma-separated names; "
                     "profiling aid, not a bench line)")
-    args = ap.parse_args()
+    ap.add_argument("--no-primitives", action="store_true",
+                    help="leave the epilogue-primitive table out of the default line")
+    ap.add_argument("--probe-ranks", action="store_true",
+                    help="start the ranks and report them, with no GPU work")
+    ap.add_argument("--backend", default="", help="process-group backend for --probe-ranks")
+    args = ap.parse_args(argv)
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be >= 1")
+    if "WORLD_SIZE" in os.environ:
+        if int(os.environ["WORLD_SIZE"]) != args.gpus:
+            raise SystemExit(f"--gpus {args.gpus} does not match WORLD_SIZE "
+                             f"{os.environ['WORLD_SIZE']} (one rank per GPU)")
+    elif args.gpus > 1:
+        sys.exit(launch_ranks(args.gpus, argv))
     if args.warmup < 3:
         print("note: at least 3 warm-up steps are required; using 3", file=sys.stderr)
         args.warmup = 3
-    if args.kernel_case:
+    if args.probe_ranks:
+        run_probe_ranks(args)
+    elif args.kernel_case:
         run_kernel_case(args)
     elif args.profile_pass:
         run_profile_pass(args)

@@ -38,6 +38,7 @@ EXPORTS = {
     "coda_col_tiles": (_I, [_I]),
     "coda_row_tiles32": (_I, [_I]),
     "coda_set_timeout_ms": (None, [_I]),
+    "coda_debug_skip_kblock": (None, [_I]),
     "coda_get_device_error": (_I, [_P]),
     "coda_last_error_string": (ctypes.c_char_p, []),
     "coda_gemm": (_I, [_P, _I, _I, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P]),

@@ -21,6 +21,7 @@ __device__ int g_coda_err;  // device error word, one per device
 
 thread_local std::string t_last_error;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<int> g_skip_kb{-1};  // coda_debug_skip_kblock
 
 // Every host-side error message lands here; with the environment variable
 // CODA_DEBUG set to anything but "0" (read once) it is also written to
@@ -105,6 +106,7 @@ coda_status_t launch_ctx(cudaStream_t st, LaunchCtx& lc) {
   lc.err = static_cast<int*>(p);
   lc.timeout_ns = g_timeout_ns.load();
   lc.num_sms = di.num_sms;
+  lc.skip_kb = g_skip_kb.load();
   return CODA_OK;
 }
 
@@ -133,10 +135,11 @@ bool map_a(CUtensorMap* m, const void* A, int lda, int transA, int M, int K) {
   return tmap2d(m, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, lda, 64, 64,
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
+// Both forms load 64 x 64 boxes; the kernel issues as many as its tile needs.
 bool map_b(CUtensorMap* m, const void* B, int ldb, int transB, int N, int K) {
   if (!transB) return tmap2d(m, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, ldb, 64, 64,
                              CU_TENSOR_MAP_SWIZZLE_128B);
-  return tmap2d(m, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, ldb, 64, kTileN / 2,
+  return tmap2d(m, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, ldb, 64, 64,
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
 // Epilogue boxes of 32 rows: 32 bf16 (64 B), 16 bf16 (32 B), 64 bf16 (128 B), 32 fp32 (128 B).
@@ -203,7 +206,7 @@ void set_last_error(const char* msg) { note_host_error(msg); }
 extern "C" {
 
 int coda_version(void) { return 100; }
-int coda_col_tiles(int N) { return N <= 0 ? 0 : (N + kTileN - 1) / kTileN; }
+int coda_col_tiles(int N) { return N <= 0 ? 0 : (N + kRowPartCols - 1) / kRowPartCols; }
 int coda_row_tiles32(int M) { return M <= 0 ? 0 : (M + 31) / 32; }
 void coda_set_timeout_ms(int ms) {
   if (ms < 1) ms = 1;
@@ -211,6 +214,8 @@ void coda_set_timeout_ms(int ms) {
 }
 
 const char* coda_last_error_string(void) { return t_last_error.c_str(); }
+
+void coda_debug_skip_kblock(int kb) { g_skip_kb.store(kb >= 0 ? kb : -1); }
 
 coda_status_t coda_get_device_error(coda_stream_t stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -383,9 +388,11 @@ coda_status_t coda_rope_table(float* cos_sin, int seq_len, int head_dim, double 
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+static int ce_tiles(int V) { return (V + kCeTileN - 1) / kCeTileN; }
+
 size_t coda_lmhead_ce_workspace_size(int M, int V) {
   if (M <= 0 || V <= 0) return 0;
-  return align256((size_t)coda_col_tiles(V) * M * sizeof(float2)) + align256((size_t)M * sizeof(float));
+  return align256((size_t)ce_tiles(V) * M * sizeof(float2)) + align256((size_t)M * sizeof(float));
 }
 
 coda_status_t coda_lmhead_ce(const void* hidden, const void* W, const int32_t* targets, float* lse,
@@ -407,7 +414,7 @@ coda_status_t coda_lmhead_ce(const void* hidden, const void* W, const int32_t* t
   CEArgs p{};
   CHECK_MAP(map_a(&p.tmA, hidden, d, 0, M, d));
   CHECK_MAP(map_b(&p.tmB, W, V, 0, V, d));
-  const int nparts = coda_col_tiles(V);
+  const int nparts = ce_tiles(V);
   p.targets = targets;
   p.part = static_cast<float2*>(ws);
   p.tlogit = reinterpret_cast<float*>(static_cast<char*>(ws) +
@@ -483,8 +490,8 @@ coda_status_t coda_lmhead_ce_bwd(const void* hidden, const void* W, const int32_
     // (2) dhidden (+)= G W_chunk^T, fp32, accumulated over the chunks
     PlainArgs h{};
     CHECK_MAP(map_a(&h.tmA, ws, chunk, 0, M, vc));
-    CHECK_MAP(tmap2d(&h.tmB, Wb + v0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vc, d, V, 64,
-                     kTileN / 2, CU_TENSOR_MAP_SWIZZLE_128B));
+    CHECK_MAP(tmap2d(&h.tmB, Wb + v0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vc, d, V, 64, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
     CHECK_MAP(map_f32_32(&h.tmC, dhidden, M, d, d));
     h.resid_ptr = v0 > 0 ? dhidden : nullptr;
     h.ld_res = (size_t)d * 4;

@@ -7,12 +7,16 @@
 //                                              per-column sums (warp transpose)
 //   (5) stateful transforms                 -- running max / sum-exp per row
 //
-// Each epilogue warp owns 32 rows of the 128 x BN accumulator tile (its TMEM
-// lane quarter) and walks the tile in chunks of 32 accumulator columns:
+// Each epilogue warp owns 32 rows (its TMEM lane quarter) and COLS columns
+// (the tile's width, or one half of it) of the 128 x BN accumulator tile,
+// passed to tile<COLS>() as the absolute first column n0 and the TMEM address
+// of that column, and walks them in chunks of 32 accumulator columns:
 // tcgen05.ld -> math -> st.shared into a swizzled box -> one TMA store per
 // output. Store staging alternates between two sets, so a chunk waits only
 // for the stores of chunks two or more back; epilogues with tile loads keep a
-// separate ring of load slots and issue each box several chunks ahead.
+// separate ring of load slots and issue each box several chunks ahead. Row
+// partials are written every kPartCols (128) columns, at partial index
+// column / 128, so their layout does not depend on the tile width.
 #pragma once
 #include "gemm.cuh"
 
@@ -152,6 +156,19 @@ __device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
   return v[0];
 }
 
+// End of a kPartCols-column group of a row partial: chunk `ch` (32 columns)
+// of a walk that starts at column n0 closes a group when ch % 4 == 3; the
+// group's index is its first column / kPartCols. Groups that start at or past
+// N (the ragged end of the last tile) are not written: the buffer has
+// ceil(N / kPartCols) of them.
+__device__ __forceinline__ bool part_group_end(int ch, int n0, int N, int& idx) {
+  static_assert(kPartCols == 128, "four 32-column chunks per partial group");
+  if ((ch & 3) != 3) return false;
+  const int c0 = n0 + (ch - 3) * 32;
+  idx = c0 / kPartCols;
+  return c0 < N;
+}
+
 // ------------------------------------------------------------------ plain
 // C = acc (+ resid), optional per-row sum of squares of the stored value's
 // fp32 pre-image. fp32 output rows are 128 bytes per 32 columns, bf16 64;
@@ -169,7 +186,7 @@ struct EpiPlain {
     CUtensorMap tm_c;
     const void* resid;    // [M, N] with the output's type, row stride ld_res bytes
     size_t ld_res;
-    float* rowsq;  // [tiles_n, M] when ROWSQ
+    float* rowsq;  // [ceil(N / kPartCols), M] when ROWSQ
   };
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params&, EpiCtx&, const GemmArgs&, int, int) {}
@@ -214,6 +231,11 @@ struct EpiPlain {
       if constexpr (ROWSQ) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+        int pi;
+        if (part_group_end(ch, n0, g.N, pi)) {
+          if (row < g.M) p.rowsq[(size_t)pi * g.M + row] = ss;
+          ss = 0.f;
+        }
       }
       if constexpr (OUT_F32) {
 #pragma unroll
@@ -232,9 +254,6 @@ struct EpiPlain {
       }
       ++c.cnt;
     }
-    if constexpr (ROWSQ) {
-      if (row < g.M) p.rowsq[(size_t)nb * g.M + row] = ss;
-    }
     return true;
   }
 };
@@ -243,8 +262,9 @@ struct EpiPlain {
 // GEMM 1 of GEMM-RMSNorm-GEMM ("Reading notes on CODA", s2; Listing 2
 // "Kernel Example": residual D = acc + C, block sum of squares of the
 // unscaled D, side output D * gamma[n]):
-//   h = acc + z (stored), hg = h * gamma (stored), part[nb, m] = sum_n h^2
-// With LN (the LayerNorm variant) also part2[nb, m] = sum_n h.
+//   h = acc + z (stored), hg = h * gamma (stored),
+//   part[n / 128, m] = sum of h^2 over each 128-column group
+// With LN (the LayerNorm variant) also part2[n / 128, m] = sum of h.
 // z is read straight into registers one chunk ahead (no shared-memory
 // staging, which leaves room for pipeline stages); two store sets of {h, hg}.
 template <bool LN>
@@ -256,8 +276,8 @@ struct EpiResidNormStats {
     CUtensorMap tm_h, tm_hg;
     const __nv_bfloat16* z;  // [M, N] residual, read into registers a chunk ahead
     const __nv_bfloat16* gamma;
-    float* part;   // [tiles_n, M] sums of h^2
-    float* part2;  // [tiles_n, M] sums of h (LN only)
+    float* part;   // [ceil(N / kPartCols), M] sums of h^2
+    float* part2;  // [ceil(N / kPartCols), M] sums of h (LN only)
   };
   template <int BN>
   static __device__ __forceinline__ void prefetch(const Params&, EpiCtx&, const GemmArgs&, int, int) {}
@@ -299,11 +319,16 @@ struct EpiResidNormStats {
         c.store(&p.tm_hg, gbuf, n0 + ch * 32, m0 + 32 * c.q);
         bulk_commit();
       }
+      int pi;
+      if (part_group_end(ch, n0, g.N, pi)) {
+        if (row < g.M) {
+          p.part[(size_t)pi * g.M + row] = ss;
+          if constexpr (LN) p.part2[(size_t)pi * g.M + row] = s1;
+        }
+        ss = 0.f;
+        s1 = 0.f;
+      }
       ++c.cnt;
-    }
-    if (row < g.M) {
-      p.part[(size_t)nb * g.M + row] = ss;
-      if constexpr (LN) p.part2[(size_t)nb * g.M + row] = s1;
     }
     return true;
   }
@@ -467,7 +492,7 @@ struct EpiCE {
   static constexpr int kSmemPerWarp = 0;
   struct Params {
     const int* targets;
-    float2* part;    // [tiles_n, M] (max, sumexp)
+    float2* part;    // [ceil(N / 256), M] (max, sumexp)
     float* tlogit;   // [M]
   };
   template <int BN>
@@ -475,6 +500,8 @@ struct EpiCE {
   template <int BN>
   static __device__ __forceinline__ bool tile(const Params& p, EpiCtx& c, const GemmArgs& g, int m0,
                                               int n0, int nb, uint32_t taddr) {
+    // one (max, sum-exp) partial per 256-column tile: the whole tile per warp
+    static_assert(BN == 256, "the CE partials are per 256-column tile");
     constexpr int NCH = BN / 32;
     const int row = m0 + 32 * c.q + c.lane;
     const int tgt = row < g.M ? __ldg(p.targets + row) : -1;
@@ -575,26 +602,27 @@ struct EpiCEGrad {
 // accumulated here):
 //   da = acc ; (g, u) = saved y pair (fp16) ; sg = sigmoid(g)
 //   dg = da u sg (1 + g (1 - sg)) ; du = da g sg
-//   spart[nb, m] = sum (dg g + du u) ; dyhat = r (dg, du) (bf16)
+//   spart[n / 128, m] = sum (dg g + du u) over each 128-column group of da ;
+//   dyhat = r (dg, du) (bf16)
 // Per 32-column chunk of da: one fp16 box of y (64 columns, 128-byte rows)
 // in, one bf16 box of dyhat (64 columns) out. A ring of kNL load slots keeps
 // the y box of the next chunk in flight; two store sets.
 // With LN (LayerNorm variant) two more row partials for the relocated
 // LayerNorm statistics: spart_w = sum dy w1, spart_b = sum dy b1.
-template <bool LN>
+template <bool LN, int NL = 2>
 struct EpiSwiGLUBwd {
   static constexpr int kYBufB = 4096;   // 32 rows x 64 fp16 (128-byte rows)
   static constexpr int kOBufB = 4096;   // 32 rows x 64 bf16 (128-byte rows)
-  static constexpr int kNL = 2;
+  static constexpr int kNL = NL;        // y load slots (1: no load ahead of its chunk)
   static constexpr int kSmemPerWarp = kNL * kYBufB + 2 * kOBufB;
   struct Params {
     CUtensorMap tm_y, tm_dy;
     const float* r;
-    float* spart;    // [tiles_n, M]
+    float* spart;    // [ceil(N / kPartCols), M]
     const float* w1;  // LN only, [2N]
     const float* b1;  // LN only, [2N]
-    float* spart_w;   // LN only, [tiles_n, M]
-    float* spart_b;   // LN only, [tiles_n, M]
+    float* spart_w;   // LN only, [ceil(N / kPartCols), M]
+    float* spart_b;   // LN only, [ceil(N / kPartCols), M]
   };
   static __device__ __forceinline__ void issue(const Params& p, EpiCtx& c, uint32_t k, int ycol,
                                                int m0) {
@@ -662,14 +690,20 @@ struct EpiSwiGLUBwd {
         c.store(&p.tm_dy, obuf, 2 * (n0 + ch * 32), m0 + 32 * c.q);
         bulk_commit();
       }
-      ++c.cnt;
-    }
-    if (row < g.M) {
-      p.spart[(size_t)nb * g.M + row] = ss;
-      if constexpr (LN) {
-        p.spart_w[(size_t)nb * g.M + row] = sw;
-        p.spart_b[(size_t)nb * g.M + row] = sb;
+      int pi;
+      if (part_group_end(ch, n0, g.N, pi)) {
+        if (row < g.M) {
+          p.spart[(size_t)pi * g.M + row] = ss;
+          if constexpr (LN) {
+            p.spart_w[(size_t)pi * g.M + row] = sw;
+            p.spart_b[(size_t)pi * g.M + row] = sb;
+          }
+        }
+        ss = 0.f;
+        sw = 0.f;
+        sb = 0.f;
       }
+      ++c.cnt;
     }
     return true;
   }

@@ -19,8 +19,11 @@ constexpr int kBM = 128;        // tile rows (TMEM lanes)
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kUK = 16;         // K per tcgen05.mma (kind::f16)
 constexpr int kSmemMax = 232448;
-constexpr int kEpiWarps = 4;      // epilogue warps per CTA, one per TMEM lane quarter
 constexpr int kEpiBars = 8;     // mbarriers per epilogue warp (tile loads)
+// Row partials (sums over a row's columns, e.g. of h^2) are written per
+// kPartCols columns, whatever the tile width: the partial buffers of the C
+// ABI are [ceil(N / kPartCols), M].
+constexpr int kPartCols = 128;
 
 struct GemmArgs {
   int M, N, K;
@@ -29,6 +32,9 @@ struct GemmArgs {
   int along_m;                    // 1: bands of row blocks (row index fastest inside a band)
   int* err;                       // device error word
   unsigned long long timeout_ns;  // bound on every wait
+  int skip_kb;                    // failure-detection tests only (normally -1): the
+                                  // producers do not load this k-block of their
+                                  // first tile, so the waits for it run out
 };
 
 // Per-epilogue-warp context: staging buffers, the warp's mbarriers for

@@ -4,22 +4,30 @@
 // Each CTA stages its own 128 rows of A and half (BN/2 columns) of B, so per
 // SM the shared-memory traffic per MMA and the operand bytes fetched from L2
 // are half those of a single-CTA 128 x BN tile; TMEM of each CTA holds its
-// 128 accumulator rows; every CTA's four epilogue warps drain their own
+// 128 accumulator rows; every CTA's epilogue warps drain their own
 // 128 x BN slice. Two TMEM accumulator buffers let the MMA warp fill buffer
 // b^1 while the epilogue warps drain buffer b (the sm_103a counterpart of the
-// pages' Hopper PingPong overlap).
+// pages' Hopper PingPong overlap). BN is 256 or 128: the narrower tile gives
+// twice the tiles, for outputs whose 256-wide tiles fill the SMs in too few
+// waves.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (64 + 32 EW threads, one CTA per SM):
 //   warp 0      TMA producer: this CTA's A rows and B half into a ring of stages
 //   warp 1      TMEM allocator; in the even CTA, the single thread issuing tcgen05.mma
-//   warps 2..5  epilogue: TMEM -> registers -> epilogue math -> smem -> TMA store
+//   warps 2..   EW epilogue warps: TMEM -> registers -> epilogue math -> smem ->
+//               TMA store. A warp may read only its own 32-lane TMEM quarter
+//               (warp index mod 4), so with EW = 4 each warp drains 32 rows x
+//               BN columns; with EW = 8 two warps share a quarter and each
+//               takes one 128-column half: twice the warps to hide the
+//               latency of an epilogue whose instruction stream outlasts a
+//               short-K mainloop.
 //
 // Synchronisation across the pair:
 //   full[s]   (even CTA)  both CTAs' TMA loads complete_tx here; the even
 //                          CTA's producer arms it with both CTAs' bytes
 //   empty[s]  (both)      MMA commit multicast to both CTAs frees stage s
 //   tfull[b]  (both)      MMA commit multicast: accumulator b is ready
-//   tempty[b] (even CTA)  8 arrivals (4 epilogue warps x 2 CTAs)
+//   tempty[b] (even CTA)  2 EW arrivals (every epilogue warp of both CTAs)
 //   drain     (both)      last MMA commit: nothing reads shared memory or
 //                          TMEM any more, so both CTAs may leave
 //
@@ -35,7 +43,7 @@
 
 namespace coda {
 
-template <int BN_, bool A_MN_, bool B_MN_, class Epi_, int MS_ = 1>
+template <int BN_, bool A_MN_, bool B_MN_, class Epi_, int MS_ = 1, int EW_ = 4>
 struct Gemm2Traits {
   static constexpr int BN = BN_;
   static constexpr bool A_MN = A_MN_;
@@ -44,12 +52,16 @@ struct Gemm2Traits {
   static constexpr int MS = MS_;                          // 128-row slabs of A per CTA
   static constexpr int NACC = MS == 1 ? 2 : 1;            // accumulator buffers in TMEM
   static_assert(MS == 1 || MS == 2, "MS");
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int EW = EW_;                          // epilogue warps
+  static_assert(EW == 4 || EW == 8, "EW");
+  static constexpr int ECOLS = BN / (EW / 4);             // columns per epilogue warp
+  static_assert(ECOLS % kPartCols == 0, "an epilogue warp covers whole row-partial groups");
+  static constexpr int kThreads = 64 + 32 * EW;
   static constexpr int SLAB_BYTES = kBM * kBK * 2;        // one 128-row slab of A
   static constexpr int A_BYTES = MS * SLAB_BYTES;         // this CTA's 128 * MS rows
   static constexpr int B_BYTES = (BN / 2) * kBK * 2;     // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int EPI_BYTES = Epi::kSmemPerWarp * kEpiWarps;
+  static constexpr int EPI_BYTES = Epi::kSmemPerWarp * EW;
   static constexpr int BAR_BYTES = 1024;
   static constexpr int kFit = (kSmemMax - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = kFit > 8 ? 8 : kFit;
@@ -81,9 +93,9 @@ __global__ void __launch_bounds__(T::kThreads, 1)
   auto empty = [&](int s) { return bars + 8u * (S + s); };
   auto tfull = [&](int i) { return bars + 8u * (2 * S + i); };
   auto tempty = [&](int i) { return bars + 8u * (2 * S + 2 + i); };
-  const uint32_t epibar = bars + 8u * (2 * S + 4);      // 4 warps x kEpiBars barriers
-  const uint32_t drainbar = bars + 8u * (2 * S + 4 + kEpiBars * kEpiWarps);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(barp + 8 * (2 * S + 5 + kEpiBars * kEpiWarps));
+  const uint32_t epibar = bars + 8u * (2 * S + 4);      // EW warps x kEpiBars barriers
+  const uint32_t drainbar = bars + 8u * (2 * S + 4 + kEpiBars * T::EW);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(barp + 8 * (2 * S + 5 + kEpiBars * T::EW));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -102,9 +114,9 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull(i), 1);
-      mbar_init(tempty(i), 2 * kEpiWarps);
+      mbar_init(tempty(i), 2 * T::EW);
     }
-    for (int j = 0; j < kEpiBars * kEpiWarps; ++j) mbar_init(epibar + 8u * j, 1);
+    for (int j = 0; j < kEpiBars * T::EW; ++j) mbar_init(epibar + 8u * j, 1);
     mbar_init(drainbar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -147,6 +159,15 @@ __global__ void __launch_bounds__(T::kThreads, 1)
             ok = false;
             break;
           }
+          if (kb == g.skip_kb && t == pair) {
+            // test hook: leave this stage unarmed and unloaded; the MMA
+            // issuer's wait for it, and every wait behind that, runs out
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (leader) mbar_arrive_expect_tx(full(stage), 2 * T::STAGE_BYTES);
           const uint32_t fb = mapa_shared(full(stage), lead);
           const uint32_t a_dst = sA + stage * T::A_BYTES;
@@ -170,8 +191,13 @@ __global__ void __launch_bounds__(T::kThreads, 1)
             }
           }
           if constexpr (!T::B_MN) {
-            if (!g.along_m) tma_load_2d_pair_hint(&tmB, b_dst, fb, k0, n0, pol_keep);
-            else tma_load_2d_pair(&tmB, b_dst, fb, k0, n0);
+            // 64-row boxes (the map does not depend on the tile width); two
+            // stacked boxes have the layout of one 128-row box
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j) {
+              if (!g.along_m) tma_load_2d_pair_hint(&tmB, b_dst + j * 8192, fb, k0, n0 + j * 64, pol_keep);
+              else tma_load_2d_pair(&tmB, b_dst + j * 8192, fb, k0, n0 + j * 64);
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j) {
@@ -248,7 +274,9 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
+    constexpr int EC = T::ECOLS;
     const int ew = warp - 2;
+    const int cpart = ew >> 2;  // column part of the tile (EW = 8: two 128-column halves)
     EpiCtx ctx;
     ctx.buf = sEpi + ew * T::Epi::kSmemPerWarp;
     ctx.bar0 = epibar + 8u * kEpiBars * ew;
@@ -263,20 +291,22 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     for (int t = pair; t < g.num_tiles; t += npairs, ++li) {
       int mb, nb;
       tile_coords(g, t, mb, nb);
-      const int m_cta = (mb * 2 + (int)rank) * T::MS * kBM, n0 = nb * BN;
+      const int m_cta = (mb * 2 + (int)rank) * T::MS * kBM;
+      const int n_w = nb * BN + cpart * EC;  // this warp's first column
+      const bool live = n_w < g.N;           // a part wholly past N has nothing to do
       const int acc = li % T::NACC;
-      T::Epi::template prefetch<BN>(ep, ctx, g, m_cta, n0);
+      if (live) T::Epi::template prefetch<EC>(ep, ctx, g, m_cta, n_w);
       bool ok = mbar_wait_cluster(tfull(acc), (li / T::NACC) & 1, e, 24);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int i = 0; i < T::MS && ok; ++i) {
+      for (int i = 0; i < T::MS && ok && live; ++i) {
         const int m0 = m_cta + i * kBM;
-        if (i > 0) T::Epi::template prefetch<BN>(ep, ctx, g, m0, n0);
-        const uint32_t taddr =
-            tmem_base + ((uint32_t)(32 * ctx.q) << 16) + (acc * T::MS + i) * BN;
-        ok = T::Epi::template tile<BN>(ep, ctx, g, m0, n0, nb, taddr);
+        if (i > 0) T::Epi::template prefetch<EC>(ep, ctx, g, m0, n_w);
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * ctx.q) << 16) +
+                               (acc * T::MS + i) * BN + cpart * EC;
+        ok = T::Epi::template tile<EC>(ep, ctx, g, m0, n_w, nb, taddr);
       }
       tc_fence_before();
       __syncwarp();

@@ -73,6 +73,17 @@ inline bool prefer_two_slabs(int M, int N, int K, int bn, int pairs, double epi_
   return w2 * (2.0 * kTwoSlabCost + epi_kb / kblocks) < 0.97 * w1;
 }
 
+// Epilogue warps of a one-slab launch: four (one per TMEM lane quarter, each
+// on the whole 256-column tile) or eight (two per quarter, each on one
+// 128-column half). Eight hide more of an epilogue's latency but leave fewer
+// pipeline stages (their staging comes out of the same shared memory). They
+// paid off only where the epilogue is much longer than a short-K mainloop:
+// the LayerNorm form of the SwiGLU backward at K = 2048 (0.226 against
+// 0.265 ms at M = 8192, f = 8192); the RMSNorm forms and the plain GEMMs ran
+// 1-3 % slower with eight, and the RMSNorm SwiGLU backward at K = 4096 20 %
+// slower.
+inline int pick_epi_warps(int K, bool heavy) { return heavy && K <= 2048 ? 8 : 4; }
+
 // Launch of the CTA-pair kernel: clusters of 2, grid = 2 x min(tiles,
 // co-resident pairs).
 template <class T>
@@ -124,6 +135,7 @@ cudaError_t launch_gemm2(const CUtensorMap& tmA, const CUtensorMap& tmB,
   choose_tile_order(g, kPairRows, T::BN, K, pairs);
   g.err = lc.err;
   g.timeout_ns = lc.timeout_ns;
+  g.skip_kb = lc.skip_kb;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, gemm2_kernel<T>, tmA, tmB, ep, g);

@@ -5,10 +5,13 @@
 
 namespace coda {
 
-template <bool LN>
+template <bool LN, int EW = 4>
 static cudaError_t swiglu_bwd_impl(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
-  using E = EpiSwiGLUBwd<LN>;
-  using T = Gemm2Traits<kTileN, false, false, E>;
+  // with eight epilogue warps, one y load slot per warp (no load ahead of its
+  // chunk; the other warp of the lane quarter covers the wait) keeps four
+  // pipeline stages
+  using E = EpiSwiGLUBwd<LN, EW == 8 ? 1 : 2>;
+  using T = Gemm2Traits<256, false, false, E, 1, EW>;
   typename E::Params p{};
   p.tm_y = a.tm_y;
   p.tm_dy = a.tm_dy;
@@ -22,13 +25,17 @@ static cudaError_t swiglu_bwd_impl(const SwiGLUBwdArgs& a, const LaunchCtx& lc) 
 }
 
 cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
-  return a.ln ? swiglu_bwd_impl<true>(a, lc) : swiglu_bwd_impl<false>(a, lc);
+  // the LayerNorm form's epilogue (two more n-vectors and two more row
+  // partials per chunk) is the one long enough for eight warps
+  if (!a.ln) return swiglu_bwd_impl<false>(a, lc);
+  return pick_epi_warps(a.K, true) == 8 ? swiglu_bwd_impl<true, 8>(a, lc)
+                                        : swiglu_bwd_impl<true>(a, lc);
 }
 
 template <bool LN, int MS>
 static cudaError_t norm_bwd_impl(const NormBwdArgs& a, const LaunchCtx& lc) {
   using E = EpiNormBwd<LN>;
-  using T = Gemm2Traits<kTileN, false, false, E, MS>;
+  using T = Gemm2Traits<256, false, false, E, MS>;
   typename E::Params p{};
   p.h = a.h;
   p.dres = a.dres;
@@ -48,7 +55,7 @@ static cudaError_t norm_bwd_impl(const NormBwdArgs& a, const LaunchCtx& lc) {
 
 cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc) {
   // K = 2f is long: two-slab tiles where the wave count allows
-  if (prefer_two_slabs(a.M, a.N, a.K, kTileN, lc.num_sms / 2, kEpiKbLoads))
+  if (prefer_two_slabs(a.M, a.N, a.K, 256, lc.num_sms / 2, kEpiKbLoads))
     return a.ln ? norm_bwd_impl<true, 2>(a, lc) : norm_bwd_impl<false, 2>(a, lc);
   return a.ln ? norm_bwd_impl<true, 1>(a, lc) : norm_bwd_impl<false, 1>(a, lc);
 }

@@ -8,7 +8,7 @@ namespace coda {
 template <bool LN, int MS>
 static cudaError_t resid_norm_stats_impl(const ResidNormStatsArgs& a, const LaunchCtx& lc) {
   using E = EpiResidNormStats<LN>;
-  using T = Gemm2Traits<kTileN, false, true, E, MS>;
+  using T = Gemm2Traits<256, false, true, E, MS>;
   typename E::Params p{};
   p.z = a.z;
   p.tm_h = a.tm_h;
@@ -19,17 +19,22 @@ static cudaError_t resid_norm_stats_impl(const ResidNormStatsArgs& a, const Laun
   return launch_gemm2<T>(a.tmA, a.tmB, p, a.M, a.N, a.K, lc);
 }
 
-cudaError_t launch_resid_norm_stats(const ResidNormStatsArgs& a, const LaunchCtx& lc) {
+template <bool LN>
+static cudaError_t resid_norm_stats_shape(const ResidNormStatsArgs& a, const LaunchCtx& lc) {
   // long K (e.g. the down projection feeding the next norm): two-slab tiles
-  if (prefer_two_slabs(a.M, a.N, a.K, kTileN, lc.num_sms / 2, kEpiKbLoads))
-    return a.ln ? resid_norm_stats_impl<true, 2>(a, lc) : resid_norm_stats_impl<false, 2>(a, lc);
-  return a.ln ? resid_norm_stats_impl<true, 1>(a, lc) : resid_norm_stats_impl<false, 1>(a, lc);
+  if (prefer_two_slabs(a.M, a.N, a.K, 256, lc.num_sms / 2, kEpiKbLoads))
+    return resid_norm_stats_impl<LN, 2>(a, lc);
+  return resid_norm_stats_impl<LN, 1>(a, lc);
+}
+
+cudaError_t launch_resid_norm_stats(const ResidNormStatsArgs& a, const LaunchCtx& lc) {
+  return a.ln ? resid_norm_stats_shape<true>(a, lc) : resid_norm_stats_shape<false>(a, lc);
 }
 
 template <bool LN>
 static cudaError_t rowscale_swiglu_impl(const RowScaleSwiGLUArgs& a, const LaunchCtx& lc) {
   using E = EpiRowScaleSwiGLU<LN>;
-  using T = Gemm2Traits<kTileN, false, true, E>;
+  using T = Gemm2Traits<256, false, true, E>;
   typename E::Params p{};
   p.tm_a = a.tm_a;
   p.tm_y = a.tm_y;
@@ -47,7 +52,7 @@ cudaError_t launch_rowscale_swiglu(const RowScaleSwiGLUArgs& a, const LaunchCtx&
 
 cudaError_t launch_rope(const RopeArgs& a, const LaunchCtx& lc) {
   using E = EpiRope;
-  using T = Gemm2Traits<kTileN, false, true, E>;
+  using T = Gemm2Traits<256, false, true, E>;
   E::Params p{};
   p.tm_out = a.tm_out;
   p.tm_save = a.tm_save;
@@ -62,7 +67,7 @@ cudaError_t launch_rope(const RopeArgs& a, const LaunchCtx& lc) {
 
 cudaError_t launch_ce(const CEArgs& a, const LaunchCtx& lc) {
   using E = EpiCE;
-  using T = Gemm2Traits<kTileN, false, true, E>;
+  using T = Gemm2Traits<256, false, true, E>;
   E::Params p{};
   p.targets = a.targets;
   p.part = a.part;
@@ -72,7 +77,7 @@ cudaError_t launch_ce(const CEArgs& a, const LaunchCtx& lc) {
 
 cudaError_t launch_ce_grad(const CEGradArgs& a, const LaunchCtx& lc) {
   using E = EpiCEGrad;
-  using T = Gemm2Traits<kTileN, false, true, E>;
+  using T = Gemm2Traits<256, false, true, E>;
   E::Params p{};
   p.tm_g = a.tm_g;
   p.targets = a.targets;

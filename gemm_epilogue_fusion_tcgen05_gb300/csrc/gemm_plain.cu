@@ -7,7 +7,7 @@ namespace coda {
 template <bool AMN, bool BMN, bool F32, bool R, bool Q, int MS = 1>
 static cudaError_t plain_impl(const PlainArgs& a, const LaunchCtx& lc) {
   using E = EpiPlain<F32, R, Q>;
-  using T = Gemm2Traits<kTileN, AMN, BMN, E, MS>;
+  using T = Gemm2Traits<256, AMN, BMN, E, MS>;
   typename E::Params p{};
   p.tm_c = a.tmC;
   p.resid = a.resid_ptr;
@@ -20,7 +20,7 @@ cudaError_t launch_plain_other(const PlainArgs& a, const LaunchCtx& lc);
 
 cudaError_t launch_plain(const PlainArgs& a, const LaunchCtx& lc) {
   if (!a.a_mn && a.b_mn) {
-    const bool two = prefer_two_slabs(a.M, a.N, a.K, kTileN, lc.num_sms / 2);
+    const bool two = prefer_two_slabs(a.M, a.N, a.K, 256, lc.num_sms / 2);
     if (a.out_f32) {
       if (a.resid) return plain_impl<false, true, true, true, false>(a, lc);
       return two ? plain_impl<false, true, true, false, false, 2>(a, lc)

@@ -7,7 +7,7 @@ namespace coda {
 template <bool AMN, bool BMN, bool F32, bool R = false, int MS = 1>
 static cudaError_t plain_t_impl(const PlainArgs& a, const LaunchCtx& lc) {
   using E = EpiPlain<F32, R, false>;
-  using T = Gemm2Traits<kTileN, AMN, BMN, E, MS>;
+  using T = Gemm2Traits<256, AMN, BMN, E, MS>;
   typename E::Params p{};
   p.tm_c = a.tmC;
   p.resid = a.resid_ptr;
@@ -21,7 +21,7 @@ cudaError_t launch_plain_other(const PlainArgs& a, const LaunchCtx& lc) {
   if (a.resid) {
     // C (+)= A B^T in fp32: e.g. a gradient accumulated over several launches
     if (!a.a_mn && !a.b_mn && a.out_f32) {
-      if (prefer_two_slabs(a.M, a.N, a.K, kTileN, lc.num_sms / 2))
+      if (prefer_two_slabs(a.M, a.N, a.K, 256, lc.num_sms / 2))
         return plain_t_impl<false, false, true, true, 2>(a, lc);
       return plain_t_impl<false, false, true, true>(a, lc);
     }
@@ -31,7 +31,7 @@ cudaError_t launch_plain_other(const PlainArgs& a, const LaunchCtx& lc) {
     return a.out_f32 ? plain_t_impl<false, false, true>(a, lc) : plain_t_impl<false, false, false>(a, lc);
   if (a.a_mn && a.b_mn) {
     // the weight-gradient shape: K = tokens, usually long
-    if (prefer_two_slabs(a.M, a.N, a.K, kTileN, lc.num_sms / 2))
+    if (prefer_two_slabs(a.M, a.N, a.K, 256, lc.num_sms / 2))
       return a.out_f32 ? plain_t_impl<true, true, true, false, 2>(a, lc)
                        : plain_t_impl<true, true, false, false, 2>(a, lc);
     return a.out_f32 ? plain_t_impl<true, true, true>(a, lc) : plain_t_impl<true, true, false>(a, lc);

@@ -16,6 +16,7 @@ struct LaunchCtx {
   int* err;                        // device error word
   unsigned long long timeout_ns;   // bound on every wait
   int num_sms;
+  int skip_kb;                     // coda_debug_skip_kblock (normally -1)
 };
 
 // Plain GEMM: C = op(A) op(B) (+ resid), optional per-row sum of squares.
@@ -114,9 +115,12 @@ cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc);
 // text returned by coda_last_error_string() for this thread
 void set_last_error(const char* msg);
 
-// tile width of every GEMM in the library (columns per accumulator tile)
-constexpr int kTileN = 256;
+// Rows of an A box (one CTA's slab); columns of the per-tile (max, sum-exp)
+// partials of the LM-head cross-entropy (its GEMM always runs 256-wide tiles);
+// columns per row partial of every other epilogue (kPartCols in core/gemm.cuh).
 constexpr int kTileM = 128;
+constexpr int kCeTileN = 256;
+constexpr int kRowPartCols = 128;
 
 // auxiliary kernels
 cudaError_t launch_row_rms(const float* part, int nparts, int M, float inv_d, float eps, float* r,

@@ -39,8 +39,9 @@
  *     CODA_ERR_RANGE).
  *   - Partial buffers: the GEMM epilogues write tile-local partials that a
  *     small auxiliary kernel reduces ([pith] Fig. 4 caption). Their shapes
- *     use coda_col_tiles(N) = ceil(N / 256) (one partial per 256-column
- *     tile) and coda_row_tiles32(M) = ceil(M / 32).
+ *     use coda_col_tiles(N) = ceil(N / 128) (one partial per 128 columns,
+ *     whatever tile width a kernel runs) and coda_row_tiles32(M) =
+ *     ceil(M / 32).
  */
 #ifndef CODA_H_
 #define CODA_H_
@@ -67,8 +68,8 @@ typedef struct CUstream_st* coda_stream_t;
 /* Library version (major * 10000 + minor * 100 + patch). */
 int coda_version(void);
 
-/* Number of per-tile partials per row written by the *_stats / *_bwd GEMMs
- * for an output of N columns: ceil(N / 256). */
+/* Number of row partials per row written by the *_stats / *_bwd GEMMs for an
+ * output of N columns: ceil(N / 128), one per 128-column group. */
 int coda_col_tiles(int N);
 /* Number of per-32-row partials per column of the RMSNorm weight gradient:
  * ceil(M / 32). */
@@ -77,6 +78,16 @@ int coda_row_tiles32(int M);
 /* Bound, in milliseconds, on every wait inside the kernels (default 2000).
  * A wait that runs out records CODA_ERR_TIMEOUT and the kernel returns. */
 void coda_set_timeout_ms(int ms);
+
+/* For tests of failure detection only; never set in normal use (default -1,
+ * off). With kb >= 0, every later GEMM launch leaves k-block kb of the first
+ * tile of each CTA pair unloaded, so the MMA issuer's bounded wait for it
+ * runs out (and with it the waits of the other roles): the kernel records
+ * CODA_ERR_TIMEOUT in the device error word, stops its loads, frees its
+ * TMEM and returns, and coda_get_device_error reports the timeout. Nothing
+ * faults and the context stays usable. kb < 0 switches it off. The setting
+ * is process-wide. */
+void coda_debug_skip_kblock(int kb);
 
 /* Synchronises `stream`, then returns and clears the device error word:
  * CODA_OK, CODA_ERR_TIMEOUT (a bounded wait ran out),
@@ -102,7 +113,7 @@ const char* coda_last_error_string(void);
  *   transB = 0: B is [K, N] (ldb >= N); 1: B is stored [N, K] (ldb >= K).
  *   resid (nullable, [M, N] of C's type, row stride ldc) is added in fp32
  *   before rounding; rowsq_part (nullable, fp32 [coda_col_tiles(N), M]) receives
- *   sum over each 256-column tile of the fp32 result squared.
+ *   the sum over each 128-column group of the fp32 result squared.
  *   c_fp32 = 1: C is fp32 (e.g. weight gradients), else bf16.
  *   rowsq_part requires transA = 0, transB = 0, c_fp32 = 0. resid requires
  *   transA = 0; with c_fp32 = 0 it is bf16 and needs transB = 0, with
@@ -116,8 +127,8 @@ coda_status_t coda_gemm(const void* A, int lda, int transA, const void* B, int l
  * output, RMSNorm-weight side output):
  *   h  = x W0 + z             (bf16 [M, N], the residual stream)
  *   hg = h * gamma[n]         (bf16 [M, N], input of the next GEMM)
- *   part[t, m] = sum over columns of tile t of h[m, n]^2 (fp32, before
- *                rounding h), part is [coda_col_tiles(N), M]
+ *   part[t, m] = sum over columns 128 t .. 128 t + 127 of h[m, n]^2 (fp32,
+ *                before rounding h), part is [coda_col_tiles(N), M]
  * x bf16 [M, K]; W0 bf16 [K, N]; z bf16 [M, N]; gamma bf16 [N]. */
 coda_status_t coda_gemm_resid_norm_stats(const void* x, const void* W0, const void* z,
                                          const void* gamma, void* h, void* hg, float* part,
@@ -246,7 +257,8 @@ coda_status_t coda_lmhead_ce_bwd(const void* hidden, const void* W, const int32_
  *   da = dout W2^T ; (g, u) = y_save pair ; sg = sigmoid(g)
  *   dg = da u sg (1 + g (1 - sg)) ; du = da g sg
  *   dyhat[m, 2k..2k+1] = r[m] (dg, du)            (bf16 [M, 2f])
- *   spart[t, m] = sum over tile t of dg g + du u  (fp32 [coda_col_tiles(f), M])
+ *   spart[t, m] = sum of dg g + du u over da columns 128 t .. 128 t + 127
+ *                                                 (fp32 [coda_col_tiles(f), M])
  * dout bf16 [M, d]; W2 bf16 [f, d]; y fp16 [M, 2f] (as saved by
  * coda_gemm_rowscale_swiglu); r fp32 [M]. */
 coda_status_t coda_gemm_rowscale_swiglu_bwd(const void* dout, const void* W2, const void* y,

@@ -41,8 +41,9 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_size_queries(L):
-    assert L.coda_col_tiles(2048) == 8
-    assert L.coda_col_tiles(2049) == 9
+    assert L.coda_col_tiles(2048) == 16
+    assert L.coda_col_tiles(2049) == 17
+    assert L.coda_col_tiles(128) == 1
     assert L.coda_col_tiles(0) == 0
     assert L.coda_row_tiles32(8192) == 256
     assert L.coda_row_tiles32(33) == 2
@@ -154,7 +155,7 @@ def test_every_entry_point_rejects_empty_and_negative_rows(L):
                             "coda_row_tiles32", "coda_lmhead_ce_workspace_size",
                             "coda_lmhead_ce_bwd_workspace_size", "coda_lmhead_ce_noalloc_capacity",
                             "coda_last_error_string",
-                            "coda_get_device_error", "coda_set_timeout_ms",
+                            "coda_get_device_error", "coda_set_timeout_ms", "coda_debug_skip_kblock",
                             "coda_selftest_bounded_wait", "coda_version")}
     assert compute <= covered, sorted(compute - covered)
 

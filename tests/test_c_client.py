@@ -20,7 +20,7 @@ def test_header_compiles(tmp_path, lang):
     if cc is None:
         pytest.skip("no host compiler")
     src = tmp_path / ("h.c" if lang == "c99" else "h.cpp")
-    src.write_text('#include "coda.h"\nint main(void) { return coda_col_tiles(256) == 1 ? 0 : 1; }\n')
+    src.write_text('#include "coda.h"\nint main(void) { return coda_col_tiles(128) == 1 ? 0 : 1; }\n')
     r = subprocess.run([cc, f"-std={lang}", "-Wall", "-Wextra", "-Werror", "-pedantic",
                         "-fsyntax-only", "-I", INC, str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr

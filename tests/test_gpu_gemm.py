@@ -184,6 +184,35 @@ def test_fp32_accumulation_matches_the_tensor_core_model(coda, MNK, scale_b):
     assert e_gpu <= e_model and abs(bias_gpu) <= abs(bias_model)
 
 
+@pytest.mark.parametrize("MNK,skip", [((512, 512, 256), 1), ((600, 1000, 1024), 5)])
+def test_production_gemm_wait_runs_out_and_recovers(coda, MNK, skip):
+    """The producers of a real GEMM launch leave one k-block of their first
+    tile unloaded (coda_debug_skip_kblock): the MMA issuer's wait for it runs
+    out under a 50 ms limit, the other roles follow through the CTA's abort
+    flag or their own limits, every CTA drains its copies, frees its TMEM and
+    returns, and the host reads CODA_ERR_TIMEOUT. The same GEMM then runs
+    normally on the same context and matches fp64 (TMEM was released)."""
+    M, N, K = MNK
+    A, B = _rand((M, K), 61), _rand((K, N), 62, 0.1)
+    Ad, Bd = A.cuda(), B.cuda()
+    C = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    coda.set_timeout_ms(50)
+    coda.lib().coda_debug_skip_kblock(skip)
+    try:
+        coda.coda_gemm(Ad, Bd, C)
+        st = coda.get_device_error()
+    finally:
+        coda.lib().coda_debug_skip_kblock(-1)
+        coda.set_timeout_ms(2000)
+    assert st == coda.CODA_ERR_TIMEOUT, f"status {st}"
+    assert b"bounded wait" in coda.lib().coda_last_error_string()
+    assert coda.get_device_error() == 0  # reading the word cleared it
+    C.fill_(float("nan"))
+    coda.coda_gemm(Ad, Bd, C)
+    assert coda.get_device_error() == 0
+    assert_close(f"gemm after a timed-out launch {MNK}", C, to64(A) @ to64(B), TOL_BF16)
+
+
 def test_bounded_wait_gives_up_without_fault(coda):
     st = coda.coda_selftest_bounded_wait(20)
     assert st == coda.CODA_ERR_TIMEOUT

@@ -1,6 +1,10 @@
 """The N > 1 path of bench.py on the CPU: two gloo ranks (127.0.0.1), each
 with its own step time, agree on the slowest one, and the job throughput
-counts every replica's work against that time."""
+counts every replica's work against that time; `bench.py --gpus 2` started
+without torchrun starts both ranks itself, each on its own device index, and
+only rank 0 prints; a --gpus that disagrees with WORLD_SIZE is refused."""
+import json
+import subprocess
 import os
 import socket
 import sys
@@ -57,3 +61,39 @@ def test_single_process_is_unchanged():
     import bench
     assert bench.max_over_ranks(3.5, "cpu") == 3.5
     assert bench.job_throughput(2e12, 1, 2.0) == pytest.approx(1000.0)
+
+
+def _bench(args, env_extra=None, timeout=300):
+    env = dict(os.environ)
+    for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], env=env,
+                          capture_output=True, text=True, timeout=timeout)
+
+
+def test_bench_starts_its_own_ranks_without_torchrun():
+    r = _bench(["--gpus", "2", "--probe-ranks", "--backend", "gloo"])
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout  # rank 0 alone prints
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["backend"] == "gloo"
+    ranks = sorted(line["ranks"], key=lambda x: x["rank"])
+    assert [x["rank"] for x in ranks] == [0, 1]
+    assert [x["device_index"] for x in ranks] == [0, 1]  # one GPU per rank (LOCAL_RANK)
+    assert ranks[0]["pid"] != ranks[1]["pid"]
+
+
+def test_single_gpu_probe_needs_no_process_group():
+    r = _bench(["--probe-ranks"])
+    assert r.returncode == 0, r.stderr
+    line = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][0])
+    assert line["n_gpus"] == 1 and line["ranks"][0]["device_index"] == 0
+
+
+def test_gpus_must_match_world_size():
+    r = _bench(["--gpus", "3", "--probe-ranks", "--backend", "gloo"],
+               {"WORLD_SIZE": "2", "RANK": "0", "LOCAL_RANK": "0"})
+    assert r.returncode != 0
+    assert "does not match WORLD_SIZE" in r.stderr
