@@ -36,6 +36,15 @@ library special cases, brute force on tiny inputs). The relative-error study
 of the pages' Fig. 6 prints no values; the GPU test checks only its
 qualitative claim (the rewritten path's error is below the PyTorch path's),
 so that one comparison has no value pin.
+
+The rewritten forms also run in an fp32 mode (``fp32=True``: GEMMs through
+the tensor-core model ``tc_matmul``, elementwise work in fp32). It is not a
+reference for the GPU: it measures how far fp32 arithmetic by itself moves
+the chained backward statistics from their fp64 values, which is where the
+tests take their bound for those statistics from
+(tests/golden/make_stat_spread.py). ``tc_matmul`` is pinned by closed forms
+(exact sums, the truncation point, the truncation bound) in
+tests/test_oracle_pins.py.
 """
 from __future__ import annotations
 
@@ -92,14 +101,13 @@ def _store_saved(store_bf16: bool):
 def tc_matmul(a, b, group: int = 16) -> np.ndarray:
     """A model of a tensor-core GEMM with an fp32 accumulator, for operands
     that are exact in fp32 (bf16 / fp16 values): along K, each group of
-    `group` products is summed exactly (in fp64, which holds these sums
-    without rounding for the sizes used here) and added to the fp32
+    `group` products is summed in fp64 (exact up to rounding far below
+    fp32's for the value ranges of these workloads) and added to the fp32
     accumulator, and that addition rounds toward zero (drops the bits below
     fp32's 24-bit significand). Truncating accumulation is what the fp32
-    results of a GEMM on this hardware show: their error is biased toward
-    zero and some twenty times a round-to-nearest fp32 GEMM's; this model
-    errs slightly more than the hardware (a GPU test checks both). Returns
-    fp32 values."""
+    results of a GB300 GEMM show: their error is biased toward zero and some
+    twenty times a round-to-nearest fp32 GEMM's; this model errs slightly
+    more than the GB300 does (a GPU test checks both). Returns fp32 values."""
     a = np.asarray(a, dtype=f64)
     b = np.asarray(b, dtype=f64)
     keep = np.uint64(0xFFFFFFFFE0000000)  # sign, exponent, top 23 fraction bits
