@@ -340,45 +340,75 @@ class Step:
         outs = [self.o2["loss"], self.o2["lse"], self.b1["dgamma"]]
         return ins, outs
 
-    def input_groups(self):
-        """The step's per-step inputs in the order the step first reads them,
-        each group with the first call that reads any of its tensors."""
-        groups = [([self.i1["x"], self.i1["z"]], "1b.gemm_resid_norm_stats"),
-                  ([self.i2["hidden"], self.i2["targets"]], "lmhead_ce"),
-                  ([self.i1["dout"]], "1b.gemm_rowscale_swiglu_bwd")]
+    def input_slots(self):
+        """Every per-step input as (dict, key), grouped by the first call that
+        reads the group. The calls look their tensors up in these dicts when
+        they run, so replacing an entry switches a call to another buffer."""
+        groups = [([(self.i1, "x"), (self.i1, "z")], "1b.gemm_resid_norm_stats"),
+                  ([(self.i2, "hidden"), (self.i2, "targets")], "lmhead_ce"),
+                  ([(self.i1, "dout")], "1b.gemm_rowscale_swiglu_bwd")]
         if self.with_8b:
-            groups += [([self.i4["o"], self.i4["z"]], "8b.gemm_resid_norm_stats(Wo)"),
-                       ([self.i4["dqkv"], self.i4["dres"]], "8b.rope_bwd")]
+            groups += [([(self.i4, "o"), (self.i4, "z")], "8b.gemm_resid_norm_stats(Wo)"),
+                       ([(self.i4, "dqkv"), (self.i4, "dres")], "8b.rope_bwd")]
         return groups
 
-    def run_from_host(self, h_groups, h_outs, copy_stream):
-        """One end-to-end step: each input group is copied host -> device on
-        `copy_stream` (after everything already queued on the compute
-        stream), and the compute stream waits for a group only right before
-        the first call that reads it, so the copies of later groups overlap
-        the kernels of earlier ones. The results are read back at the end."""
-        main = torch.cuda.current_stream()
-        copy_stream.wait_stream(main)
-        first = {}
-        for gi, (group, name) in enumerate(self.input_groups()):
-            ev = torch.cuda.Event()
+    def input_groups(self):
+        """The step's per-step input tensors in the order the step first
+        reads them, each group with the first call that reads any of them."""
+        return [([d[k] for d, k in slots], name) for slots, name in self.input_slots()]
+
+    def _use_inputs(self, tensors):
+        flat = [dk for slots, _ in self.input_slots() for dk in slots]
+        for (d, k), t in zip(flat, tensors):
+            d[k] = t
+
+    def run_e2e(self, steps, h_ins, h_outs, copy_stream, flush, stream):
+        """End-to-end steps through the public calls: every step copies its
+        inputs host -> device from pinned memory (`h_ins`, in input_groups
+        order) and reads its results back into `h_outs`. Two device buffer
+        sets hold the inputs: while step i computes on one, step i + 1's
+        inputs are copied into the other on `copy_stream` (once step i - 1 has
+        finished reading it), the prefetching input pipeline of a training
+        loop; step 0's copy is not overlapped. Returns one event pair per step
+        on `stream` (the L2 flush before each step is outside its pair); the
+        buffers the step held before are restored at the end."""
+        first = [t for g, _ in self.input_groups() for t in g]
+        sets = [first, [torch.empty_like(t) for t in first]]
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        done = [torch.cuda.Event(), torch.cuda.Event()]
+        outs = self.host_io()[1]
+
+        def copy_into(dst, ev):
             with torch.cuda.stream(copy_stream):
-                for hsrc, ddst in zip(h_groups[gi], group):
+                for hsrc, ddst in zip(h_ins, dst):
                     ddst.copy_(hsrc, non_blocking=True)
                 ev.record(copy_stream)
-            first.setdefault(name, []).append(ev)
-        pending = [ev for evs in first.values() for ev in evs]
-        for name, fl, fn, nl in self.calls:
-            for ev in first.pop(name, []):
-                main.wait_event(ev)
-            fn()
-        for evs in first.values():  # groups whose reader is not in this step
-            for ev in evs:
-                main.wait_event(ev)
-        outs = self.host_io()[1]
-        for dsrc, hdst in zip(outs, h_outs):
-            hdst.copy_(dsrc, non_blocking=True)
-        return pending
+
+        evs = []
+        for i in range(steps):
+            flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            cur = i % 2
+            if i == 0:
+                copy_stream.wait_stream(stream)
+                copy_into(sets[0], copied[0])
+            self._use_inputs(sets[cur])
+            stream.wait_event(copied[cur])
+            if i + 1 < steps:
+                nxt = 1 - cur
+                if i >= 1:
+                    copy_stream.wait_event(done[nxt])  # step i - 1 is done with that set
+                copy_into(sets[nxt], copied[nxt])
+            for name, fl, fn, nl in self.calls:
+                fn()
+            done[cur].record(stream)
+            for dsrc, hdst in zip(outs, h_outs):
+                hdst.copy_(dsrc, non_blocking=True)
+            e1.record(stream)
+            evs.append((e0, e1))
+        self._use_inputs(sets[0])
+        return evs
 
 
 def run_coda(args):
@@ -462,28 +492,19 @@ def run_coda(args):
     # Run right after the timed region, for the same number of steps and
     # with its own clock record, so that both legs see the same power state.
     ins, outs = step.host_io()
-    h_groups = [[t.cpu().pin_memory() for t in group] for group, _ in step.input_groups()]
+    h_ins = [t.cpu().pin_memory() for t in ins]
     h_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    h2d = sum(t.numel() * t.element_size() for g in h_groups for t in g)
+    h2d = sum(t.numel() * t.element_size() for t in h_ins)
     d2h = sum(t.numel() * t.element_size() for t in h_outs)
     e2e_steps = 0 if args.only else args.steps
     copy_stream = torch.cuda.Stream(device=dev)
-    for _ in range(2 if e2e_steps else 0):  # untimed: first uses of the copy stream
-        step.run_from_host(h_groups, h_outs, copy_stream)
+    if e2e_steps:
+        step.run_e2e(2, h_ins, h_outs, copy_stream, flush, stream)  # untimed first use
     torch.cuda.synchronize()
-    # The steps are enqueued back to back, as in the device-timed leg: each
-    # step's copies wait for the previous step's readers of the same buffers
-    # (run_from_host), and the host synchronises once at the end, so a host
-    # stall shorter than the queued work does not show in the step times.
+    # the steps are enqueued back to back, as in the device-timed leg, with
+    # one host synchronisation at the end
     te0 = time.time()
-    e2e_ev = []
-    for i in range(e2e_steps):
-        flush.fill_(float(i))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step.run_from_host(h_groups, h_outs, copy_stream)
-        e1.record(stream)
-        e2e_ev.append((e0, e1))
+    e2e_ev = step.run_e2e(e2e_steps, h_ins, h_outs, copy_stream, flush, stream) if e2e_steps else []
     torch.cuda.synchronize()
     te1 = time.time()
     e2e_ms_list = [a.elapsed_time(b) for a, b in e2e_ev]
@@ -542,9 +563,9 @@ def run_coda(args):
                 "step_ms": [round(t, 3) for t in e2e_ms_list],
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "each step's activations, upstream gradients and targets copied "
-                          "host -> device from pinned memory per input group on a copy stream "
-                          "(compute waits for a group only before its first reader); the "
-                          "weights stay resident on the device and are not copied; the "
+                          "host -> device from pinned memory on a copy stream into one of two "
+                          "device buffer sets, a step ahead (step 0's copy not overlapped); the "
+                          "weights stay resident on the device and are not copied; each step's "
                           "losses and dgamma are read back",
                 "timing": "the same number of steps as the timed region, run right after it, "
                           "enqueued back to back with one host synchronisation at the end",

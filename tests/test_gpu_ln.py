@@ -182,3 +182,39 @@ def test_resid_stats_long_k(coda, ln):
     if ln:
         assert_close("sum h partials (long K)", psum.cpu()[:, rows], tiles.sum(axis=2).T,
                      TOL_F32)
+
+
+@pytest.mark.parametrize("d", [2048, 2560])
+def test_ln_swiglu_bwd_both_epilogue_forms(coda, d):
+    """The LayerNorm SwiGLU backward GEMM runs eight epilogue warps at
+    K = d <= 2048 and four above: both forms against the rewritten oracle
+    on the same kind of inputs (M = 512, f = 1024, ragged-free): dyhat and
+    the three row partials per 128 da columns (sum dy y, sum dy w1,
+    sum dy b1)."""
+    M, f = 512, 1024
+    g = torch.Generator().manual_seed(90 + d)
+    dout = torch.randn(M, d, generator=g).to(torch.bfloat16)
+    W2 = (torch.randn(f, d, generator=g) * 0.02).to(torch.bfloat16)
+    y = torch.randn(M, 2 * f, generator=g).to(torch.float16)
+    r = torch.rand(M, generator=g) + 0.5
+    w1 = torch.randn(2 * f, generator=g) * 0.1
+    b1 = torch.randn(2 * f, generator=g) * 0.1
+    cu = {k: v.cuda() for k, v in dict(dout=dout, W2=W2, y=y, r=r, w1=w1, b1=b1).items()}
+    dyhat = torch.empty(M, 2 * f, dtype=torch.bfloat16, device="cuda")
+    parts = [torch.empty(coda.col_tiles(f), M, dtype=torch.float32, device="cuda") for _ in range(3)]
+    coda.coda_gemm_ln_rowscale_swiglu_bwd(cu["dout"], cu["W2"], cu["y"], cu["r"], cu["w1"], cu["b1"],
+                                          dyhat, *parts)
+    torch.cuda.synchronize()
+    assert coda.get_device_error() == 0
+    n = {k: O.to64(v) for k, v in dict(dout=dout, W2=W2, y=y, r=r, w1=w1, b1=b1).items()}
+    z = np.zeros
+    fwd = {"h": z((M, d)), "hg": z((M, d)), "mu": z(M), "r": n["r"], "w1": n["w1"], "b1": n["b1"],
+           "y": n["y"], "a": z((M, f))}
+    ref = O.ln_mlp_bwd_reparam(fwd, z((M, d)), z((d, d)), z((d, 2 * f)), n["W2"], np.ones(d),
+                               z(d), n["dout"], store_bf16=True)
+    assert_close(f"dyhat (d={d})", dyhat, ref["dyhat"], TOL_BF16)
+    dy = ref["dy"]
+    for name, got, vec in (("sum dy y", parts[0], n["y"]), ("sum dy w1", parts[1], n["w1"][None, :]),
+                           ("sum dy b1", parts[2], n["b1"][None, :])):
+        want = (dy * vec).reshape(M, -1, 256).sum(axis=2).T  # 128 da columns = 256 y columns
+        assert_close(f"{name} partials (d={d})", got, want, TOL_F32)
