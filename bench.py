@@ -489,8 +489,9 @@ def run_coda(args):
 
     # end-to-end through the public API with host buffers: copy this step's
     # inputs host -> device from pinned memory, run, read the results back.
-    # Run right after the timed region, for the same number of steps and
-    # with its own clock record, so that both legs see the same power state.
+    # Run after the timed region and the per-call pass (the GPU already
+    # power-capped, as in the timed region's later steps), for the same
+    # number of steps and with its own clock window.
     ins, outs = step.host_io()
     h_ins = [t.cpu().pin_memory() for t in ins]
     h_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
@@ -567,8 +568,9 @@ def run_coda(args):
                           "device buffer sets, a step ahead (step 0's copy not overlapped); the "
                           "weights stay resident on the device and are not copied; each step's "
                           "losses and dgamma are read back",
-                "timing": "the same number of steps as the timed region, run right after it, "
-                          "enqueued back to back with one host synchronisation at the end",
+                "timing": "the same number of steps as the timed region, run after it and "
+                          "the per-call pass, enqueued back to back with one host "
+                          "synchronisation at the end",
                 "clocks": clk_e2e},
         "clocks": clk,
         "step_ms_spread": {"min": round(min(step_ms), 4), "median": round(sorted(step_ms)[len(step_ms) // 2], 4),
