@@ -2,7 +2,7 @@
 
 Each .cu file compiles to an object in parallel; the objects link into one
 shared library next to this file. The CUDA runtime is linked statically, and
-the driver entry point for TMA descriptors is looked up at run time, so the
+the CUDA driver API entry point for TMA descriptors is looked up at run time, so the
 library loads on a machine without a GPU (for symbol checks) as well.
 """
 from __future__ import annotations

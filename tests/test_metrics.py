@@ -45,6 +45,6 @@ def test_stat_allowance_is_the_given_tolerance():
 def test_elementwise_rel_uses_a_floor_near_zero():
     ref = np.array([1.0, 1e-9])
     got = np.array([1.001, 2e-9])
-    # the tiny entry is judged against 1e-3 * rms(ref), not against itself
+    # the tiny entry is measured against 1e-3 * rms(ref), not against itself
     assert elementwise_rel(got, ref) == pytest.approx(1e-3, rel=1e-6)
     assert elementwise_rel(ref, ref) == 0.0
