@@ -609,7 +609,12 @@ struct EpiCEGrad {
 // the y box of the next chunk in flight; two store sets.
 // With LN (LayerNorm variant) two more row partials for the relocated
 // LayerNorm statistics: spart_w = sum dy w1, spart_b = sum dy b1.
-template <bool LN, int NL = 2>
+// HOIST: the chunk's eight y vectors are read from shared memory before any
+// of its dyhat stores, so the compiler may interleave the 32 pairs'
+// dependency chains (the shared loads and stores are ordered asm); without
+// it each group of four pairs waits for the previous group's store. Same
+// results either way.
+template <bool LN, int NL = 2, bool HOIST = false>
 struct EpiSwiGLUBwd {
   static constexpr int kYBufB = 4096;   // 32 rows x 64 fp16 (128-byte rows)
   static constexpr int kOBufB = 4096;   // 32 rows x 64 bf16 (128-byte rows)
@@ -650,6 +655,11 @@ struct EpiSwiGLUBwd {
       float da[32];
       tmem_ld32(taddr + ch * 32, da);
       if (!c.wait(slot, 12)) return false;
+      uint4 yall[8];
+      if constexpr (HOIST) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) yall[k] = ld_shared_v4(ybuf + swz<128>(c.lane, k));
+      }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {  // 16 pairs (32 y columns) at a time
         float w[32], bb[32];
@@ -660,7 +670,9 @@ struct EpiSwiGLUBwd {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // output 16-byte chunk k = pairs 4k .. 4k+3
           const int k = 4 * hh + kk;
-          const uint4 yv = ld_shared_v4(ybuf + swz<128>(c.lane, k));
+          uint4 yv;
+          if constexpr (HOIST) yv = yall[k];
+          else yv = ld_shared_v4(ybuf + swz<128>(c.lane, k));
           const float2 p0 = unpack_f16(yv.x), p1 = unpack_f16(yv.y), p2 = unpack_f16(yv.z),
                        p3 = unpack_f16(yv.w);
           const float gy[4] = {p0.x, p1.x, p2.x, p3.x};

@@ -5,12 +5,12 @@
 
 namespace coda {
 
-template <bool LN, int EW = 4>
+template <bool LN, int EW = 4, bool HOIST = false>
 static cudaError_t swiglu_bwd_impl(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
   // with eight epilogue warps, one y load slot per warp (no load ahead of its
   // chunk; the other warp of the lane quarter covers the wait) keeps four
   // pipeline stages
-  using E = EpiSwiGLUBwd<LN, EW == 8 ? 1 : 2>;
+  using E = EpiSwiGLUBwd<LN, EW == 8 ? 1 : 2, HOIST>;
   using T = Gemm2Traits<256, false, false, E, 1, EW>;
   typename E::Params p{};
   p.tm_y = a.tm_y;
@@ -27,7 +27,12 @@ static cudaError_t swiglu_bwd_impl(const SwiGLUBwdArgs& a, const LaunchCtx& lc) 
 cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
   // the LayerNorm form's epilogue (two more n-vectors and two more row
   // partials per chunk) is the one long enough for eight warps
-  if (!a.ln) return swiglu_bwd_impl<false>(a, lc);
+  // RMSNorm form: at short K the epilogue outlasts the mainloop, and reading
+  // each chunk's y ahead of its stores ran 4 % faster (M = 8192, f = 8192,
+  // K = 2048); at K = 4096 the epilogue hides behind the mainloop and the
+  // form measured no better
+  if (!a.ln) return a.K <= 2048 ? swiglu_bwd_impl<false, 4, true>(a, lc)
+                                : swiglu_bwd_impl<false>(a, lc);
   return pick_epi_warps(a.K, true) == 8 ? swiglu_bwd_impl<true, 8>(a, lc)
                                         : swiglu_bwd_impl<true>(a, lc);
 }
