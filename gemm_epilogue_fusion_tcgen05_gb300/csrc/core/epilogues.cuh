@@ -43,6 +43,26 @@ __device__ __forceinline__ void load_nvec32(const __nv_bfloat16* p, int n, int N
   }
 }
 
+// The same 32 bf16 values left packed (four 16-byte words, 16 registers), so
+// that a chunk's vector can be fetched a chunk ahead of its use; unpack with
+// unpack8. Columns >= N read as 0.
+__device__ __forceinline__ void load_nvec32_raw(const __nv_bfloat16* p, int n, int N,
+                                                uint4 (&o)[4]) {
+  if (n + 32 <= N) {
+    const uint4* q = reinterpret_cast<const uint4*>(p + n);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = __ldg(q + k);
+  } else {
+    uint32_t w[16] = {};
+    const unsigned short* h = reinterpret_cast<const unsigned short*>(p);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n + j < N) w[j >> 1] |= (uint32_t)__ldg(h + n + j) << (16 * (j & 1));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  }
+}
+
 // 32 fp32 values of an n-vector starting at column n (broadcast load).
 // Columns >= N read as 0.
 __device__ __forceinline__ void load_nvec32f(const float* p, int n, int N, float (&o)[32]) {
@@ -91,7 +111,7 @@ __device__ __forceinline__ void ldg_row(const void* base, size_t ld_bytes, int r
   }
 }
 
-// Unpack one 16-byte chunk (8 bf16) from shared memory into o[0..7].
+// Unpack one 16-byte chunk (8 bf16) into o[0..7].
 __device__ __forceinline__ void unpack8(uint4 u, float* o) {
   o[0] = bf16_lo(u.x); o[1] = bf16_hi(u.x); o[2] = bf16_lo(u.y); o[3] = bf16_hi(u.y);
   o[4] = bf16_lo(u.z); o[5] = bf16_hi(u.z); o[6] = bf16_lo(u.w); o[7] = bf16_hi(u.w);
@@ -267,6 +287,9 @@ struct EpiPlain {
 // With LN (the LayerNorm variant) also part2[n / 128, m] = sum of h.
 // z is read straight into registers one chunk ahead (no shared-memory
 // staging, which leaves room for pipeline stages); two store sets of {h, hg}.
+// gamma is fetched a chunk ahead with z: loaded in its own chunk it came from
+// L2 after the TMEM load (the asm orders the two) and was most of a chunk's
+// time.
 template <bool LN>
 struct EpiResidNormStats {
   static constexpr int kBufB = 2048;  // 32 rows x 32 bf16
@@ -288,21 +311,30 @@ struct EpiResidNormStats {
     const int row = m0 + 32 * c.q + c.lane;
     const size_t ldb = (size_t)g.N * 2;
     float ss = 0.f, s1 = 0.f;
-    uint4 zn[4];
+    uint4 zn[4], gn[4];
     ldg_row<4>(p.z, ldb, row, g.M, 2 * n0, 2 * g.N, zn);
+    load_nvec32_raw(p.gamma, n0, g.N, gn);
     for (int ch = 0; ch < NCH; ++ch) {
-      uint4 zv[4];
+      uint4 zv[4], gv[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) zv[k] = zn[k];
-      if (ch + 1 < NCH) ldg_row<4>(p.z, ldb, row, g.M, 2 * (n0 + (ch + 1) * 32), 2 * g.N, zn);
+      for (int k = 0; k < 4; ++k) {
+        zv[k] = zn[k];
+        gv[k] = gn[k];
+      }
+      if (ch + 1 < NCH) {
+        ldg_row<4>(p.z, ldb, row, g.M, 2 * (n0 + (ch + 1) * 32), 2 * g.N, zn);
+        load_nvec32_raw(p.gamma, n0 + (ch + 1) * 32, g.N, gn);
+      }
       const uint32_t hbuf = c.buf + (c.cnt & 1) * kStoreB;
       const uint32_t gbuf = hbuf + kBufB;
       c.stores_read_but_last();
       float v[32], gm[32], z[32];
       tmem_ld32(taddr + ch * 32, v);
-      load_nvec32(p.gamma, n0 + ch * 32, g.N, gm);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) unpack8(zv[k], &z[8 * k]);
+      for (int k = 0; k < 4; ++k) {
+        unpack8(gv[k], &gm[8 * k]);
+        unpack8(zv[k], &z[8 * k]);
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         v[j] += z[j];
