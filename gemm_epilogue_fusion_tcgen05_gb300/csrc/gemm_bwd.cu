@@ -37,10 +37,10 @@ cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
                                         : swiglu_bwd_impl<true>(a, lc);
 }
 
-template <bool LN, int MS>
+template <bool LN, int MS, int EW = 4>
 static cudaError_t norm_bwd_impl(const NormBwdArgs& a, const LaunchCtx& lc) {
   using E = EpiNormBwd<LN>;
-  using T = Gemm2Traits<256, false, false, E, MS>;
+  using T = Gemm2Traits<256, false, false, E, MS, EW>;
   typename E::Params p{};
   p.h = a.h;
   p.dres = a.dres;
@@ -59,9 +59,15 @@ static cudaError_t norm_bwd_impl(const NormBwdArgs& a, const LaunchCtx& lc) {
 }
 
 cudaError_t launch_norm_bwd(const NormBwdArgs& a, const LaunchCtx& lc) {
-  // K = 2f is long: two-slab tiles where the wave count allows
+  // K = 2f is long: two-slab tiles where the wave count allows. A two-slab
+  // tile fills TMEM with one accumulator, so its epilogue does not overlap
+  // the next tile's MMAs; in the RMSNorm form eight epilogue warps (column
+  // halves) shorten it and still leave four pipeline stages (2-3 % at
+  // M = 16384, d = 4096, K = 28672; 1 % at M = 8192, d = 2048, K = 16384).
+  // The one-slab form, whose epilogue overlaps, measured no better with
+  // eight; the LayerNorm form's registers do not fit eight.
   if (prefer_two_slabs(a.M, a.N, a.K, 256, lc.num_sms / 2, kEpiKbLoads))
-    return a.ln ? norm_bwd_impl<true, 2>(a, lc) : norm_bwd_impl<false, 2>(a, lc);
+    return a.ln ? norm_bwd_impl<true, 2>(a, lc) : norm_bwd_impl<false, 2, 8>(a, lc);
   return a.ln ? norm_bwd_impl<true, 1>(a, lc) : norm_bwd_impl<false, 1>(a, lc);
 }
 
