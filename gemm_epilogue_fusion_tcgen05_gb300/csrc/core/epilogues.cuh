@@ -79,13 +79,30 @@ __device__ __forceinline__ void load_nvec32f(const float* p, int n, int N, float
   }
 }
 
+// One 16-byte vector of a row at byte b0: bytes at or past row_bytes read as
+// zero, and a vector that the row ends inside is filled 2 bytes at a time.
+__device__ __forceinline__ uint4 ldg16_row(const char* rp, int b0, int row_bytes) {
+  if (b0 + 16 <= row_bytes) return __ldg(reinterpret_cast<const uint4*>(rp + b0));
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  if (b0 < row_bytes) {
+    const unsigned short* hp = reinterpret_cast<const unsigned short*>(rp + b0);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (b0 + 2 * e < row_bytes) w[e >> 1] |= (uint32_t)__ldg(hp + e) << (16 * (e & 1));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // 16 * NV consecutive bytes of one row of a row-major tensor, starting at
 // byte `col_bytes` (a multiple of 16) of the row, read straight into
-// registers with 16-byte non-coherent loads: an epilogue's input tile, read
-// one chunk ahead of its use instead of being staged in shared memory. Rows
-// >= M and bytes at or past `row_bytes` read as zero; a vector that the row
-// ends inside is filled 2 bytes at a time, so nothing past the row's last
+// registers with non-coherent loads: an epilogue's input tile, read one chunk
+// ahead of its use instead of being staged in shared memory. Rows >= M and
+// bytes at or past `row_bytes` read as zero; nothing past the row's last
 // element is read (row strides are multiples of 16 bytes, row lengths of 2).
+// Every lane reads a different row, so each load instruction is 32 separate
+// L1 requests; where the base, the row stride and col_bytes are all
+// multiples of 32 bytes the row is read 32 bytes per request
+// (ld.global.nc.v8), which halves the requests for the same bytes.
 template <int NV>
 __device__ __forceinline__ void ldg_row(const void* base, size_t ld_bytes, int row, int M,
                                         int col_bytes, int row_bytes, uint4 (&o)[NV]) {
@@ -94,20 +111,28 @@ __device__ __forceinline__ void ldg_row(const void* base, size_t ld_bytes, int r
   for (int k = 0; k < NV; ++k) o[k] = zero;
   if (row >= M) return;
   const char* rp = static_cast<const char*>(base) + (size_t)row * ld_bytes;
-  const uint4* p = reinterpret_cast<const uint4*>(rp + col_bytes);
+  const bool wide = (NV % 2) == 0 && ((reinterpret_cast<uintptr_t>(base) | (uintptr_t)ld_bytes |
+                                        (uintptr_t)col_bytes) & 31u) == 0;
+  if (wide) {
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int b0 = col_bytes + 16 * k;
-    if (b0 + 16 <= row_bytes) {
-      o[k] = __ldg(p + k);
-    } else if (b0 < row_bytes) {
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-      const unsigned short* hp = reinterpret_cast<const unsigned short*>(rp + b0);
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (b0 + 2 * e < row_bytes) w[e >> 1] |= (uint32_t)__ldg(hp + e) << (16 * (e & 1));
-      o[k] = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int k2 = 0; k2 < NV / 2; ++k2) {
+      const int b0 = col_bytes + 32 * k2;
+      if (b0 + 32 <= row_bytes) {
+        uint32_t r[8];
+        asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                       "=r"(r[6]), "=r"(r[7])
+                     : "l"(rp + b0));
+        o[2 * k2] = make_uint4(r[0], r[1], r[2], r[3]);
+        o[2 * k2 + 1] = make_uint4(r[4], r[5], r[6], r[7]);
+      } else {
+        o[2 * k2] = ldg16_row(rp, b0, row_bytes);
+        o[2 * k2 + 1] = ldg16_row(rp, b0 + 16, row_bytes);
+      }
     }
+  } else {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) o[k] = ldg16_row(rp, col_bytes + 16 * k, row_bytes);
   }
 }
 
