@@ -17,7 +17,14 @@ BLOCKS = [WORKLOADS["tiny_mlp_fwd"],
           BlockShape("ragged", M=200, d=136, f=200, seed=11),
           BlockShape("multi_tile", M=384, d=520, f=392, seed=12),
           # one token: every 256-row pair tile holds a single valid row
-          BlockShape("one_row", M=1, d=64, f=64, seed=13)]
+          BlockShape("one_row", M=1, d=64, f=64, seed=13),
+          # rows of 1056 bytes: the epilogues' 32-byte row loads, with a last
+          # chunk of 16 columns that falls back to 16-byte loads
+          BlockShape("wide_ragged", M=300, d=528, f=264, seed=14),
+          # K = 2f = 12320 over 80 tiles: the RMSNorm-backward GEMM takes the
+          # two-slab tile with eight epilogue warps, on ragged M and d (the
+          # SwiGLU backward, K = d = 1040, its short-K form)
+          BlockShape("two_slab_ragged", M=4000, d=1040, f=6160, seed=15)]
 
 
 @pytest.fixture(scope="module")

@@ -119,21 +119,23 @@ def test_gemm_resid_rowsq(coda, MNK):
     assert_close("row sum of squares", part.sum(0), np.sum(ref * ref, axis=1), 1e-3)
 
 
-@pytest.mark.parametrize("c_fp32", [0, 1])
-def test_gemm_resid_row_ends_inside_a_vector(coda, c_fp32):
-    """The epilogue reads the residual straight into registers, 16 bytes at a
-    time; here each row ends inside such a vector (N = 260 bf16 / 262 fp32,
-    inside row strides of 264 elements), so the last elements come from the
-    partial-vector path."""
+@pytest.mark.parametrize("c_fp32,ld", [(0, 264), (1, 264), (0, 272)])
+def test_gemm_resid_row_ends_inside_a_vector(coda, c_fp32, ld):
+    """The epilogue reads the residual straight into registers, 32 bytes at a
+    time where the row stride is a multiple of 32 bytes and 16 otherwise;
+    here each row ends inside such a vector (N = 260 bf16 / 262 fp32), so the
+    last elements come from the partial-vector path. Row strides of 264
+    elements: 528 bytes (bf16, 16-byte loads) and 1056 bytes (fp32, 32-byte
+    loads); 272 bf16 elements: 544 bytes (32-byte loads)."""
     M, K = 200, 72
     N = 262 if c_fp32 else 260
     dt = torch.float32 if c_fp32 else torch.bfloat16
-    A, Bbig = _rand((M, K), 17), _rand((K, 264), 18, 0.1)
-    B = Bbig[:, :N]  # row stride 264 elements (16-byte multiple)
+    A, Bbig = _rand((M, K), 17), _rand((K, ld), 18, 0.1)
+    B = Bbig[:, :N]  # row stride ld elements (16-byte multiple)
     g = torch.Generator().manual_seed(19)
-    Rbig = torch.full((M, 264), float("nan"), dtype=dt)
+    Rbig = torch.full((M, ld), float("nan"), dtype=dt)
     Rbig[:, :N] = torch.randn(M, N, generator=g).to(dt)
-    Cbig = torch.zeros((M, 264), dtype=dt, device="cuda")
+    Cbig = torch.zeros((M, ld), dtype=dt, device="cuda")
     Rd = Rbig.cuda()
     if c_fp32:  # C += A B: the residual is C itself
         Cbig[:, :N] = Rd[:, :N]
