@@ -25,14 +25,14 @@ static cudaError_t swiglu_bwd_impl(const SwiGLUBwdArgs& a, const LaunchCtx& lc) 
 }
 
 cudaError_t launch_swiglu_bwd(const SwiGLUBwdArgs& a, const LaunchCtx& lc) {
-  // the LayerNorm form's epilogue (two more n-vectors and two more row
-  // partials per chunk) is the one long enough for eight warps
   // RMSNorm form: at short K the epilogue outlasts the mainloop, and reading
   // each chunk's y ahead of its stores ran 4 % faster (M = 8192, f = 8192,
   // K = 2048); at K = 4096 the epilogue hides behind the mainloop and the
   // form measured no better
   if (!a.ln) return a.K <= 2048 ? swiglu_bwd_impl<false, 4, true>(a, lc)
                                 : swiglu_bwd_impl<false>(a, lc);
+  // the LayerNorm form's epilogue (two more n-vectors and two more row
+  // partials per chunk) is the one long enough for eight warps
   return pick_epi_warps(a.K, true) == 8 ? swiglu_bwd_impl<true, 8>(a, lc)
                                         : swiglu_bwd_impl<true>(a, lc);
 }
